@@ -1,0 +1,185 @@
+"""ctypes wrapper of the fp64 C oracle of the routed MoE layer (moe_oracle.c).
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT.  Only the tests, the smoke check
+and the benchmark's CPU-baseline / reference leg import this package.  The CUDA
+library never calls it and shares no code with it.
+
+``build()`` compiles moe_oracle.c with gcc into ``oracle/libmoe_oracle.so``
+(in-tree, git-ignored).  The functions below take numpy arrays (bf16/fp16 as
+uint16 bit patterns) and return numpy arrays.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "moe_oracle.c")
+LIB = os.path.join(HERE, "libmoe_oracle.so")
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(
+            os.path.getmtime(SRC), os.path.getmtime(os.path.join(HERE, "moe_oracle.h"))):
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, SRC, "-lm"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = C.CDLL(LIB)
+        _lib.mo_bf16_to_f64.restype = C.c_double
+        _lib.mo_bf16_to_f64.argtypes = [C.c_uint16]
+        _lib.mo_f16_to_f64.restype = C.c_double
+        _lib.mo_f16_to_f64.argtypes = [C.c_uint16]
+    return _lib
+
+
+def _p(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return None if a is None else np.ascontiguousarray(a, dtype=dtype)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"oracle {what} failed with code {rc}")
+
+
+def bf16_to_f64(bits: int) -> float:
+    return lib().mo_bf16_to_f64(int(bits))
+
+
+def f16_to_f64(bits: int) -> float:
+    return lib().mo_f16_to_f64(int(bits))
+
+
+def dequant(q, s, rows: int, K: int) -> np.ndarray:
+    q, s = _c(q, np.uint8), _c(s, np.uint16)
+    w = np.empty((rows, K), dtype=np.float64)
+    _check(lib().mo_dequant(_p(q), _p(s), rows, K, _p(w)), "dequant")
+    return w
+
+
+def router_logits(x, W_r, g=None) -> np.ndarray:
+    x, W_r, g = _c(x, np.uint16), _c(W_r, np.uint16), _c(g, np.uint16)
+    T, H = x.shape
+    E = W_r.shape[0]
+    out = np.empty((T, E + (g is not None)), dtype=np.float64)
+    _check(lib().mo_router_logits(_p(x), _p(W_r), _p(g), T, H, E, _p(out)), "router_logits")
+    return out
+
+
+def router_topk(logits, k: int, E: Optional[int] = None):
+    logits = _c(logits, np.float64)
+    T, ld = logits.shape
+    E = ld if E is None else E
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    _check(lib().mo_router_topk(_p(logits), ld, T, E, k, _p(ids), _p(w)), "router_topk")
+    return ids, w
+
+
+def dispatch(ids, E: int):
+    ids = _c(ids, np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    perm = np.empty(T * k, dtype=np.int32)
+    inv = np.empty(T * k, dtype=np.int32)
+    _check(lib().mo_dispatch(_p(ids), T, k, E, _p(counts), _p(offsets), _p(perm), _p(inv)), "dispatch")
+    return counts, offsets, perm, inv
+
+
+def expert_row(x_row, gate, up, down, H: int, I: int) -> np.ndarray:
+    """gate/up/down: (q, s) pairs of one expert."""
+    x_row = _c(x_row, np.uint16)
+    arrs = [_c(gate[0], np.uint8), _c(gate[1], np.uint16), _c(up[0], np.uint8), _c(up[1], np.uint16),
+            _c(down[0], np.uint8), _c(down[1], np.uint16)]
+    o = np.empty(H, dtype=np.float64)
+    _check(lib().mo_expert_row(_p(x_row), H, I, *[_p(a) for a in arrs], _p(o)), "expert_row")
+    return o
+
+
+def _exp_ptrs(ex):
+    arrs = [_c(ex.gate.q, np.uint8), _c(ex.gate.s, np.uint16), _c(ex.up.q, np.uint8),
+            _c(ex.up.s, np.uint16), _c(ex.down.q, np.uint8), _c(ex.down.s, np.uint16)]
+    return arrs
+
+
+def expert_mlp(x, ex, ids, perm, token_mask=None) -> np.ndarray:
+    x, ids, perm = _c(x, np.uint16), _c(ids, np.int32), _c(perm, np.int32)
+    T, H = x.shape
+    k = ids.shape[1]
+    arrs = _exp_ptrs(ex)
+    tm = _c(token_mask, np.uint8)
+    rows = np.zeros((T * k, H), dtype=np.float64)
+    _check(lib().mo_expert_mlp(_p(x), T, H, ex.I, ex.E, k, *[_p(a) for a in arrs],
+                               _p(ids), _p(perm), _p(tm), _p(rows)), "expert_mlp")
+    return rows
+
+
+def shared_expert(x, sh, token_mask=None) -> np.ndarray:
+    x = _c(x, np.uint16)
+    T, H = x.shape
+    arrs = _exp_ptrs(sh)
+    g = _c(sh.g, np.uint16)
+    tm = _c(token_mask, np.uint8)
+    y = np.zeros((T, H), dtype=np.float64)
+    _check(lib().mo_shared_expert(_p(x), T, H, sh.I_sh, *[_p(a) for a in arrs], _p(g), _p(tm), _p(y)),
+           "shared_expert")
+    return y
+
+
+def combine(rows, inv, w, shared=None, residual=None, token_mask=None) -> np.ndarray:
+    rows, inv, w = _c(rows, np.float64), _c(inv, np.int32), _c(w, np.float64)
+    shared, residual = _c(shared, np.float64), _c(residual, np.uint16)
+    T, k = w.shape
+    H = rows.shape[1]
+    tm = _c(token_mask, np.uint8)
+    y = np.zeros((T, H), dtype=np.float64)
+    _check(lib().mo_combine(_p(rows), _p(inv), _p(w), _p(shared), _p(residual), T, k, H, _p(tm), _p(y)),
+           "combine")
+    return y
+
+
+def layer_forward(inp, token_mask=None):
+    """inp: mixture_experts_layer_09_gb300.inputs.LayerInputs.  Returns dict with the fp32-rounded
+    router logits, ids, w and y (fp64)."""
+    wl = inp.wl
+    x = _c(inp.x, np.uint16)
+    T, H = x.shape
+    ex, sh = inp.experts, inp.shared
+    arrs = _exp_ptrs(ex)
+    if sh is not None:
+        sarrs = _exp_ptrs(sh)
+        sg = _c(sh.g, np.uint16)
+        I_sh = sh.I_sh
+    else:
+        sarrs, sg, I_sh = [None] * 6, None, 0
+    tm = _c(token_mask, np.uint8)
+    logits = np.empty((T, ex.E), dtype=np.float64)
+    ids = np.empty((T, wl.k), dtype=np.int32)
+    w = np.empty((T, wl.k), dtype=np.float64)
+    y = np.zeros((T, H), dtype=np.float64)
+    r = _c(inp.residual, np.uint16)
+    W_r = _c(inp.W_r, np.uint16)
+    _check(lib().mo_layer_forward(_p(x), _p(r), _p(W_r), T, H, ex.I, ex.E, wl.k,
+                                  *[_p(a) for a in arrs], I_sh, *[_p(a) for a in sarrs], _p(sg), _p(tm),
+                                  _p(logits), _p(ids), _p(w), _p(y)), "layer_forward")
+    return {"logits": logits, "ids": ids, "w": w, "y": y}

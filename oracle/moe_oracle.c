@@ -1,0 +1,306 @@
+/*
+ * moe_oracle.c -- plain fp64 CPU oracle of the routed Mixture-of-Experts layer.
+ *
+ * TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT (see moe_oracle.h).  Written for
+ * a reader checking it against the pages by eye: one loop per definition, fp64
+ * throughout, no blocking, fusion or reordering.  Single-threaded.
+ *
+ * Parity pins (tests/test_oracle_pins.py): brute-force full sort for top-k,
+ * hand-decoded nibbles, closed forms of the MLP, dispatch invariants, the
+ * zero-weight invariance of the combine, and tests/golden fixtures.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* bf16 is the top half of an IEEE binary32; widening is exact. */
+double mo_bf16_to_f64(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* IEEE binary16, decoded field by field (normal, subnormal, inf/nan). */
+double mo_f16_to_f64(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int ex = (bits >> 10) & 0x1F;
+    int man = bits & 0x3FF;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)man, -24);              /* man/1024 * 2^-14 */
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp(1.0 + (double)man / 1024.0, ex - 15);
+    return sign ? -v : v;
+}
+
+/* One weight element of an int4 matrix (colibri #418, "Correctness": int4 is
+ * offset-binary, value = nibble - 8, in the CPU byte layout; "Grouped scales in
+ * the Vulkan kernels": one scale per group of K-columns, here 32). */
+static double weight_at(const uint8_t* q, const uint16_t* s, int K, int n, int c) {
+    uint8_t byte = q[(size_t)n * (K / 2) + c / 2];
+    int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
+    return (double)(nib - 8) * mo_f16_to_f64(s[(size_t)n * (K / 32) + c / 32]);
+}
+
+int mo_dequant(const uint8_t* q, const uint16_t* s, int rows, int K, double* w) {
+    if (!q || !s || !w || rows < 0 || K <= 0 || K % 32) return -1;
+    for (int n = 0; n < rows; ++n)
+        for (int c = 0; c < K; ++c)
+            w[(size_t)n * K + c] = weight_at(q, s, K, n, c);
+    return 0;
+}
+
+/* Router logits: one GEMV row per expert over the hidden row, and the shared
+ * expert's gate logit as one more row "past the router's logits"
+ * (dasLLAMA #3988, decode span and routed-block commits). */
+int mo_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
+                     int T, int H, int E, double* logits) {
+    if (!x || !W_r || !logits || T < 0 || H <= 0 || E <= 0) return -1;
+    int ld = E + (g ? 1 : 0);
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += mo_bf16_to_f64(x[(size_t)t * H + h]) * mo_bf16_to_f64(W_r[(size_t)e * H + h]);
+            logits[(size_t)t * ld + e] = acc;
+        }
+        if (g) {
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += mo_bf16_to_f64(x[(size_t)t * H + h]) * mo_bf16_to_f64(g[h]);
+            logits[(size_t)t * ld + E] = acc;
+        }
+    }
+    return 0;
+}
+
+/* Softmax top-k router (vllm.cpp #481, warp-router commit: softmax over the
+ * row, pick k with a -inf mask, lowest index wins a tie; dasLLAMA #3988,
+ * routed-block commit: per-row top-k "renormalized").  k rounds of argmax over
+ * the unmasked experts with a strict '>' so the lowest index keeps a tie; the
+ * picks are then written in ascending expert id.  Weights: the full softmax
+ * over all E logits, renormalised over the k picks. */
+int mo_router_topk(const double* logits, int ld, int T, int E, int k,
+                   int32_t* ids, double* w) {
+    if (!logits || !ids || !w || T < 0 || E <= 0 || ld < E || k < 1 || k > E) return -1;
+    unsigned char* picked = (unsigned char*)malloc((size_t)E);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    if (!picked || !p) { free(picked); free(p); return -1; }
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; ++t) {
+        const double* l = logits + (size_t)t * ld;
+        for (int e = 0; e < E; ++e)
+            if (!isfinite(l[e])) rc = -2;
+        if (rc) break;
+        memset(picked, 0, (size_t)E);
+        for (int round = 0; round < k; ++round) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!picked[e] && (best < 0 || l[e] > l[best])) best = e;
+            picked[best] = 1;
+        }
+        double m = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > m) m = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) p[e] = exp(l[e] - m) / z;
+        double psel = 0.0;
+        for (int e = 0; e < E; ++e)
+            if (picked[e]) psel += p[e];
+        int j = 0;
+        for (int e = 0; e < E; ++e) {
+            if (!picked[e]) continue;
+            ids[(size_t)t * k + j] = e;
+            w[(size_t)t * k + j] = p[e] / psel;
+            ++j;
+        }
+    }
+    free(picked);
+    free(p);
+    return rc;
+}
+
+/* Bucket schedule (dasLLAMA #3988, routed-block commit: thread e counts expert
+ * e's slots, exclusive scans place the buckets, the slot map lands in slot
+ * order).  counts[e] = #{slots a : ids[a] == e}; offsets = exclusive scan with
+ * offsets[E] = T*k; perm lists, bucket by bucket, the slots a in ascending
+ * order; inv[perm[r]] = r. */
+int mo_dispatch(const int32_t* ids, int T, int k, int E, int32_t* counts,
+                int32_t* offsets, int32_t* perm, int32_t* inv) {
+    if (!ids || !counts || !offsets || !perm || !inv || T < 0 || k < 1 || E <= 0) return -1;
+    int n = T * k;
+    for (int a = 0; a < n; ++a)
+        if (ids[a] < 0 || ids[a] >= E) return -1;
+    for (int e = 0; e < E; ++e) {
+        counts[e] = 0;
+        for (int a = 0; a < n; ++a)
+            if (ids[a] == e) ++counts[e];
+    }
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    int r = 0;
+    for (int e = 0; e < E; ++e)
+        for (int a = 0; a < n; ++a)
+            if (ids[a] == e) perm[r++] = a;
+    for (int q = 0; q < n; ++q) inv[perm[q]] = q;
+    return 0;
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* The fused expert group "gate+up+silu->down" (colibri #418, "Summary"):
+ * g = W_g x, u = W_u x, h = silu(g) * u, o = W_d h. */
+int mo_expert_row(const uint16_t* x_row, int H, int I,
+                  const uint8_t* gq, const uint16_t* gs,
+                  const uint8_t* uq, const uint16_t* us,
+                  const uint8_t* dq, const uint16_t* ds, double* o) {
+    if (!x_row || !gq || !gs || !uq || !us || !dq || !ds || !o) return -1;
+    if (H <= 0 || I <= 0 || H % 32 || I % 32) return -1;
+    double* h = (double*)malloc(sizeof(double) * (size_t)I);
+    if (!h) return -1;
+    for (int i = 0; i < I; ++i) {
+        double g = 0.0, u = 0.0;
+        for (int c = 0; c < H; ++c) {
+            double xv = mo_bf16_to_f64(x_row[c]);
+            g += weight_at(gq, gs, H, i, c) * xv;
+            u += weight_at(uq, us, H, i, c) * xv;
+        }
+        h[i] = silu(g) * u;
+    }
+    for (int n = 0; n < H; ++n) {
+        double acc = 0.0;
+        for (int i = 0; i < I; ++i) acc += weight_at(dq, ds, I, n, i) * h[i];
+        o[n] = acc;
+    }
+    free(h);
+    return 0;
+}
+
+int mo_expert_mlp(const uint16_t* x, int T, int H, int I, int E, int k,
+                  const uint8_t* gate_q, const uint16_t* gate_s,
+                  const uint8_t* up_q, const uint16_t* up_s,
+                  const uint8_t* down_q, const uint16_t* down_s,
+                  const int32_t* ids, const int32_t* perm,
+                  const uint8_t* token_mask, double* rows) {
+    if (!x || !ids || !perm || !rows || T < 0 || E <= 0 || k < 1) return -1;
+    size_t gq_sz = (size_t)I * (H / 2), gs_sz = (size_t)I * (H / 32);
+    size_t dq_sz = (size_t)H * (I / 2), ds_sz = (size_t)H * (I / 32);
+    for (int r = 0; r < T * k; ++r) {
+        int a = perm[r], t = a / k, e = ids[a];
+        if (e < 0 || e >= E) return -1;
+        if (token_mask && !token_mask[t]) continue;
+        int rc = mo_expert_row(x + (size_t)t * H, H, I,
+                               gate_q + e * gq_sz, gate_s + e * gs_sz,
+                               up_q + e * gq_sz, up_s + e * gs_sz,
+                               down_q + e * dq_sz, down_s + e * ds_sz,
+                               rows + (size_t)r * H);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/* Shared expert scaled by sigmoid of its gate logit; an ungated shared expert
+ * adds at weight one (dasLLAMA #3988, decode span commit). */
+int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,
+                     const uint8_t* gate_q, const uint16_t* gate_s,
+                     const uint8_t* up_q, const uint16_t* up_s,
+                     const uint8_t* down_q, const uint16_t* down_s,
+                     const uint16_t* g, const uint8_t* token_mask, double* y_sh) {
+    if (!x || !y_sh || T < 0) return -1;
+    for (int t = 0; t < T; ++t) {
+        if (token_mask && !token_mask[t]) continue;
+        const uint16_t* xr = x + (size_t)t * H;
+        int rc = mo_expert_row(xr, H, I_sh, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                               y_sh + (size_t)t * H);
+        if (rc) return rc;
+        double gate = 1.0;
+        if (g) {
+            double z = 0.0;
+            for (int h = 0; h < H; ++h) z += mo_bf16_to_f64(xr[h]) * mo_bf16_to_f64(g[h]);
+            gate = 1.0 / (1.0 + exp(-z));
+        }
+        for (int n = 0; n < H; ++n) y_sh[(size_t)t * H + n] *= gate;
+    }
+    return 0;
+}
+
+/* Combine onto the residual (dasLLAMA #3988: the routed slots weighted by the
+ * top-k weights, plus the gated shared row, onto the residual).  In fp64 the
+ * summation order is immaterial; the pages' order (shared, slots, residual)
+ * is kept anyway. */
+int mo_combine(const double* rows, const int32_t* inv, const double* w,
+               const double* shared, const uint16_t* residual,
+               int T, int k, int H, const uint8_t* token_mask, double* y) {
+    if (!rows || !inv || !w || !y || T < 0 || k < 1 || H <= 0) return -1;
+    for (int t = 0; t < T; ++t) {
+        if (token_mask && !token_mask[t]) continue;
+        for (int n = 0; n < H; ++n) {
+            double acc = shared ? shared[(size_t)t * H + n] : 0.0;
+            for (int j = 0; j < k; ++j) {
+                int a = t * k + j;
+                acc += w[a] * rows[(size_t)inv[a] * H + n];
+            }
+            if (residual) acc += mo_bf16_to_f64(residual[(size_t)t * H + n]);
+            y[(size_t)t * H + n] = acc;
+        }
+    }
+    return 0;
+}
+
+int mo_layer_forward(const uint16_t* x, const uint16_t* residual,
+                     const uint16_t* W_r, int T, int H, int I, int E, int k,
+                     const uint8_t* gate_q, const uint16_t* gate_s,
+                     const uint8_t* up_q, const uint16_t* up_s,
+                     const uint8_t* down_q, const uint16_t* down_s,
+                     int I_sh,
+                     const uint8_t* sh_gate_q, const uint16_t* sh_gate_s,
+                     const uint8_t* sh_up_q, const uint16_t* sh_up_s,
+                     const uint8_t* sh_down_q, const uint16_t* sh_down_s,
+                     const uint16_t* sh_g, const uint8_t* token_mask,
+                     double* logits_out, int32_t* ids_out, double* w_out, double* y) {
+    if (!x || !W_r || !y || T < 0 || k < 1 || k > E) return -1;
+    size_t nslot = (size_t)T * k;
+    double* logits = (double*)malloc(sizeof(double) * ((size_t)T * E + 1));
+    int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (nslot + 1));
+    double* w = (double*)malloc(sizeof(double) * (nslot + 1));
+    int32_t* counts = (int32_t*)malloc(sizeof(int32_t) * (size_t)E);
+    int32_t* offsets = (int32_t*)malloc(sizeof(int32_t) * ((size_t)E + 1));
+    int32_t* perm = (int32_t*)malloc(sizeof(int32_t) * (nslot + 1));
+    int32_t* inv = (int32_t*)malloc(sizeof(int32_t) * (nslot + 1));
+    double* rows = (double*)calloc(nslot * (size_t)H + 1, sizeof(double));
+    double* ysh = I_sh > 0 ? (double*)calloc((size_t)T * H + 1, sizeof(double)) : NULL;
+    int rc = -1;
+    if (!logits || !ids || !w || !counts || !offsets || !perm || !inv || !rows || (I_sh > 0 && !ysh))
+        goto done;
+    rc = mo_router_logits(x, W_r, NULL, T, H, E, logits);
+    if (rc) goto done;
+    /* the router consumes fp32 logits: round before selection */
+    for (size_t i = 0; i < (size_t)T * E; ++i) logits[i] = (double)(float)logits[i];
+    if (logits_out) memcpy(logits_out, logits, sizeof(double) * (size_t)T * E);
+    rc = mo_router_topk(logits, E, T, E, k, ids, w);
+    if (rc) goto done;
+    rc = mo_dispatch(ids, T, k, E, counts, offsets, perm, inv);
+    if (rc) goto done;
+    rc = mo_expert_mlp(x, T, H, I, E, k, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                       ids, perm, token_mask, rows);
+    if (rc) goto done;
+    if (I_sh > 0) {
+        rc = mo_shared_expert(x, T, H, I_sh, sh_gate_q, sh_gate_s, sh_up_q, sh_up_s,
+                              sh_down_q, sh_down_s, sh_g, token_mask, ysh);
+        if (rc) goto done;
+    }
+    rc = mo_combine(rows, inv, w, ysh, residual, T, k, H, token_mask, y);
+    if (rc) goto done;
+    if (ids_out) memcpy(ids_out, ids, sizeof(int32_t) * nslot);
+    if (w_out) memcpy(w_out, w, sizeof(double) * nslot);
+done:
+    free(logits); free(ids); free(w); free(counts); free(offsets);
+    free(perm); free(inv); free(rows); free(ysh);
+    return rc;
+}
