@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE layer on one GB300: tokens/s and us/layer.
+
+Workload: the Qwen3-30B-A3B-shaped decode layer (H=2048, I=768, E=128, top-k=8, no shared
+expert, int4 nibble-8 experts with fp16 scales per 32 columns), batch T=16 tokens, synthetic
+seeded inputs.  A step = one moe_layer_forward call (router logits, softmax top-k, dispatch,
+fused int4 expert MLP with the combine in the down projection) on one batch.  Weights stay
+resident in HBM; L2 reuse between steps is defeated by cycling 4 independent layer replicas
+(340 MB of experts each, 4 x 340 MB > 4 x L2) and 16 distinct input batches.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.  Multi-GPU (torchrun) runs independent replicas, one per
+rank: the layer has no cross-GPU exchange, so no collective touches the data path.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from mixture_experts_layer_09_gb300 import inputs as gen  # noqa: E402
+
+METRIC = "MoE-layer tokens/s & us/layer at 1 GB300; % of HBM (decode) / TC (prefill) roof"
+WORKLOAD = dict(name="qwen3_30b_a3b_decode_moe_layer", H=2048, I=768, E=128, k=8, T=16)
+SWEEP_T = (1, 4)
+N_REPLICAS = 4
+N_INPUTS = 16
+BYTES_PER_EXPERT = lambda H, I: 3 * (H * I // 2) + 3 * (H * I // 32) * 2  # noqa: E731
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, path, gpu_index):
+        self.path, self.proc, self.gpu = path, None, gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank):
+    """The fp64 CPU oracle as it stands, timed on the host cores: each step is one token of
+    the benchmark batch (routing of the whole batch, then that token's experts and combine)."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    wl = gen.Workload(WORKLOAD["name"], WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["I"], WORKLOAD["E"], WORKLOAD["k"])
+    inp = gen.draw_layer(wl)
+    T = wl.T
+
+    def step(i):
+        mask = np.zeros(T, dtype=np.uint8)
+        mask[i % T] = 1
+        oracle.layer_forward(inp, token_mask=mask)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    tps = args.steps / dt
+    line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{wl.name} H={wl.H} I={wl.I} E={wl.E} k={wl.k} T={wl.T}",
+                       "impl_note": "fp64 C oracle, single thread"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps of 1 token of the T={T} batch"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def upload_layer(torch, moe, inp):
+    def dev(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(dtype) if dtype is not None else t).cuda()
+
+    def q4(m):
+        return moe.Q4(dev(m.q), dev(m.s.view(np.int16), torch.float16))
+
+    ex = inp.experts
+    E = moe.Experts(ex.E, ex.H, ex.I, q4(ex.gate), q4(ex.up), q4(ex.down))
+    return dev(inp.W_r.view(np.int16), torch.bfloat16), E
+
+
+def time_loop(torch, fn, steps, warmup):
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        fn(warmup + i)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import mixture_experts_layer_09_gb300 as moe
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    moe.build()
+    H, I, E, k, T = WORKLOAD["H"], WORKLOAD["I"], WORKLOAD["E"], WORKLOAD["k"], WORKLOAD["T"]
+    seed0 = 1000 * rank
+
+    # ---- resident weights: independent layer replicas
+    layers = []
+    for rep in range(N_REPLICAS):
+        ex = gen.draw_experts(seed0 + rep, E, H, I)
+        Wr = gen.draw_router(seed0 + rep, E, H)
+        inp = gen.LayerInputs(gen.Workload("b", T, H, I, E, k), None, None, Wr, ex, None)
+        W_r, Ed = upload_layer(torch, moe, inp)
+        layers.append(moe.MoeLayer(W_r, Ed, None, k, max_T=T))
+        del ex, inp
+
+    def inputs(Tb):
+        xs = [gen.draw_x(seed0 + 500 + i, Tb, H) for i in range(N_INPUTS)]
+        rs = [gen.draw_residual(seed0 + 700 + i, Tb, H) for i in range(N_INPUTS)]
+        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
+        return [to(x).cuda() for x in xs], [to(r).cuda() for r in rs], [to(x).pin_memory() for x in xs], \
+            [to(r).pin_memory() for r in rs]
+
+    def measure(Tb, steps, warmup, full=False):
+        xd, rd, xh, rh = inputs(Tb)
+        y = torch.empty((Tb, H), dtype=torch.float32, device="cuda")
+        ids = torch.empty((Tb, k), dtype=torch.int32, device="cuda")
+
+        def step(i):
+            layers[i % N_REPLICAS].forward(xd[i % N_INPUTS], rd[i % N_INPUTS], y=y, topk_ids_out=ids)
+
+        out = {}
+        if dist is not None:
+            dist.barrier()
+        n0 = moe.moe_launch_count()
+        clocks = Clocks(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
+                                     else ".", f"clocks_bench_r{rank}_T{Tb}.csv"), local)
+        if full:
+            clocks.start()
+        dt = time_loop(torch, step, steps, warmup)
+        if full:
+            out["clocks"] = clocks.stop()
+        out["launches_per_step"] = (moe.moe_launch_count() - n0) / (steps + warmup)
+        if dist is not None:
+            t = torch.tensor([dt], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        out["plain_s"] = dt
+        # CUDA-graph replay of the same steps (one graph per (replica, input) pair)
+        graphs = []
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step(0)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for i in range(N_INPUTS):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(i)
+            graphs.append(g)
+        dtg = time_loop(torch, lambda i: graphs[i % N_INPUTS].replay(), steps, warmup)
+        if dist is not None:
+            t = torch.tensor([dtg], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dtg = float(t.item())
+        out["graph_s"] = dtg
+        # distinct experts per step (routing is the GPU's own output)
+        nd = []
+        for i in range(N_INPUTS):
+            step(i)
+            torch.cuda.synchronize()
+            nd.append(len(np.unique(ids.cpu().numpy())))
+        out["n_distinct"] = nd
+        if full:
+            # per-kernel device time over a timed pass, CUDA events on the launching stream
+            moe.moe_profile_enable(True)
+            time_loop(torch, step, steps, 0)
+            out["kernels"] = moe.moe_profile_read()
+            moe.moe_profile_enable(False)
+            # end to end through host buffers: H2D of x and residual, D2H of y, every step
+            yh = torch.empty((Tb, H), dtype=torch.float32).pin_memory()
+            xin = torch.empty((Tb, H), dtype=torch.bfloat16, device="cuda")
+            rin = torch.empty((Tb, H), dtype=torch.bfloat16, device="cuda")
+
+            def e2e_step(i):
+                xin.copy_(xh[i % N_INPUTS], non_blocking=True)
+                rin.copy_(rh[i % N_INPUTS], non_blocking=True)
+                layers[i % N_REPLICAS].forward(xin, rin, y=y)
+                yh.copy_(y, non_blocking=True)
+
+            dte = time_loop(torch, e2e_step, steps, warmup)
+            if dist is not None:
+                t = torch.tensor([dte], device="cuda")
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                dte = float(t.item())
+            out["e2e_s"] = dte
+            out["h2d"] = 2 * Tb * H * 2
+            out["d2h"] = Tb * H * 4
+        return out
+
+    main = measure(T, args.steps, args.warmup, full=True)
+    sweep = {}
+    for Tb in SWEEP_T:
+        r = measure(Tb, max(10, args.steps // 2), args.warmup)
+        best = min(r["plain_s"], r["graph_s"])
+        us = 1e6 * best / max(10, args.steps // 2)
+        sweep[f"T={Tb}"] = {"us_per_layer": us, "tokens_per_s": Tb / (us * 1e-6),
+                            "plain_us": 1e6 * r["plain_s"] / max(10, args.steps // 2),
+                            "graph_us": 1e6 * r["graph_s"] / max(10, args.steps // 2)}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    steps = args.steps
+    best_s = min(main["plain_s"], main["graph_s"])
+    ms_step = 1e3 * best_s / steps
+    value = world * T * steps / best_s
+    hbm, tc, src = peaks()
+    # roofline of the dominant kernel (by device time)
+    kern = main["kernels"]
+    dom = max(kern, key=lambda n: kern[n][0])
+    dom_ms = kern[dom][0] / max(kern[dom][1], 1)
+    nd = float(np.mean(main["n_distinct"]))
+    bpe = BYTES_PER_EXPERT(H, I)
+    per_kernel_bytes = {
+        "gateup_gemv": nd * (2 * I * H // 2 + 2 * I * (H // 32) * 2) + T * H * 2 + T * (H // 32) * 8 + T * k * I * 4,
+        "down_gemv_combine": nd * (H * I // 2 + H * (I // 32) * 2) + T * k * I * 2 + T * k * (I // 32) * 8
+        + T * H * 2 + T * H * 4,
+    }
+    ach = per_kernel_bytes.get(dom, float("nan")) / (dom_ms * 1e-3) / 1e9
+    layer_bytes = nd * bpe + E * H * 2 + T * H * (2 + 2 + 4)
+    layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD['name']} H={H} I={I} E={E} k={k} T={T}", "global_batch": T * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{N_REPLICAS} layer replicas x {E * bpe / 1e6:.0f} MB of experts cycled with "
+                         f"{N_INPUTS} distinct batches (inputs larger than L2)",
+                   "us_per_layer": ms_step * 1e3,
+                   "plain_us_per_layer": 1e6 * main["plain_s"] / steps,
+                   "graph_us_per_layer": 1e6 * main["graph_s"] / steps,
+                   "mean_distinct_experts": nd,
+                   "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm,
+                   "sweep": sweep},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                     "frac": ach / hbm, "peak_source": src, "traffic": None,
+                     "kernel_us": dom_ms * 1e3},
+        "kernels_us_per_step": {n: 1e3 * v[0] / steps for n, v in kern.items()},
+        "gpu_launches": int(round(main["launches_per_step"] * steps)),
+        "clocks": main.get("clocks"),
+        "e2e": {"value": world * T * steps / main["e2e_s"], "unit": "tokens/s",
+                "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
+    }
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        wl = gen.Workload(WORKLOAD["name"], T, H, I, E, k)
+        inp = gen.draw_layer(wl)
+        n_tok = 4
+        mask = np.zeros(T, dtype=np.uint8)
+        mask[:n_tok] = 1
+        t0 = time.perf_counter()
+        oracle.layer_forward(inp, token_mask=mask)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n_tok} tokens of the T={T} batch (routing for all {T})"}
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * moe.h -- C ABI of the routed Mixture-of-Experts layer for one GB300 (sm_103a).
+ *
+ * The layer (four stages):
+ *   1. softmax top-k router: fp32 softmax over E expert logits, top-k with the
+ *      lowest index winning a tie, weights renormalised over the k picks
+ *      [vllm.cpp PR #481 "gate(#378): the first DEVICE run of the warp MoE
+ *      router", warp-router commit; daScript PR #3988 "dasLLAMA vulkan: a MoE
+ *      that fits the card ...", routed-block commit: TopKRows];
+ *   2. token-to-expert dispatch: per-expert histogram, exclusive scan, stable
+ *      permutation [daScript PR #3988, routed-block commit: MoeSched];
+ *   3. grouped SwiGLU expert MLP over int4 offset-binary weights (value =
+ *      nibble - 8) with one fp16 scale per 32 K-columns: gate+up, silu(gate)*up,
+ *      down [colibri PR #418 "Vulkan backend: expert tier + dense + MLA
+ *      attention on any Vulkan 1.2 GPU", Summary, Correctness and "Grouped
+ *      scales in the Vulkan kernels"];
+ *   4. weighted combine onto the residual plus an optional shared expert scaled
+ *      by sigmoid(x . g) [daScript PR #3988, decode span commit: DecCombineSh;
+ *      the combine-folded residual commit: shared row, then the slots in
+ *      order, then the residual].
+ *
+ * Conventions for every entry point
+ *   - Pointers to tensors are DEVICE pointers, owned by the caller; the library
+ *     never frees or retains them.  Struct pointers (moe_experts, moe_shared)
+ *     and `status` out-parameters are HOST pointers, read/written during the
+ *     call only.
+ *   - bf16 and fp16 tensors are passed as uint16_t bit patterns.  Tensors are
+ *     dense row-major with the shapes stated per argument.
+ *   - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the legacy
+ *     default stream).  Every call only enqueues work on `stream`, returns
+ *     without synchronising, and allocates no device memory: scratch comes from
+ *     the caller's workspace `ws` of at least the size the matching
+ *     *_workspace_size() function returns (256-byte aligned).
+ *   - Arguments are validated on the host before any launch; a failed check
+ *     returns MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED and enqueues nothing.
+ *     A launch failure returns MOE_ERR_CUDA.  No C++ exception crosses the ABI.
+ *   - Faults found on the device (a routed id outside [0, E), a bounded wait
+ *     that ran out) are recorded in a status word inside the workspace and the
+ *     kernel skips the affected work; moe_device_status() reads and clears it.
+ *   - There is no CPU fallback: without a usable sm_103a device every call that
+ *     would launch returns MOE_ERR_CUDA.
+ *
+ * Weight layout ("CPU byte layout", uploaded with a plain copy, colibri #418):
+ *   moe_q4.q  uint8  [n_mat][rows][K/2]: column c of a row is nibble (c & 1) of
+ *             byte c/2 (low nibble = even column); value = nibble - 8
+ *   moe_q4.s  fp16   [n_mat][rows][K/32]: scale of columns 32g .. 32g+31
+ *   routed experts (n_mat = E): gate, up: rows = I, K = H; down: rows = H, K = I
+ *   shared expert  (n_mat = 1): gate, up: rows = I_sh, K = H; down: rows = H, K = I_sh
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef void* moe_stream_t; /* a cudaStream_t */
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,     /* null pointer, size out of range, workspace too small */
+    MOE_ERR_UNSUPPORTED = -2,     /* valid request this build does not serve */
+    MOE_ERR_CUDA = -3,            /* a CUDA call or launch failed (no device, bad stream, ...) */
+    MOE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait ran out (recorded on device) */
+    MOE_ERR_DEVICE_INDEX = -5     /* a routed expert id outside [0, E) (recorded on device) */
+};
+
+enum {
+    MOE_ARM_AUTO = 0,  /* GEMV when T <= 32, grouped GEMM otherwise */
+    MOE_ARM_GEMV = 1,  /* bandwidth arm: fused int4 GEMV, weights streamed once per call */
+    MOE_ARM_GEMM = 2   /* tensor arm: grouped GEMM on tcgen05 / TMEM */
+};
+
+/* Size limits checked on the host. */
+#define MOE_MAX_E 256
+#define MOE_MAX_K 32
+#define MOE_MAX_T_GEMV_COMBINE 32
+
+typedef struct {
+    const uint8_t* q;   /* device, uint8 [n_mat][rows][K/2] */
+    const uint16_t* s;  /* device, fp16  [n_mat][rows][K/32] */
+} moe_q4;
+
+typedef struct {
+    int E, H, I;        /* 1 <= E <= 256; H, I positive multiples of 32 */
+    moe_q4 gate, up, down;
+} moe_experts;
+
+typedef struct {
+    int I_sh;           /* positive multiple of 32 */
+    moe_q4 gate, up, down;
+    const uint16_t* g;  /* device, bf16 [H] gate vector; NULL = ungated (weight 1) */
+} moe_shared;
+
+/* Text of a status code (static storage). */
+MOE_API const char* moe_status_string(int status);
+
+/* Library version string, e.g. "moe-gb300 0.1 sm_103a". */
+MOE_API const char* moe_version(void);
+
+/* Router logits (stage 1, its GEMV/GEMM: one dot product per expert row and,
+ * when g != NULL, one more row for the shared-expert gate "landing past the
+ * router's logits", daScript PR #3988 decode span commit).
+ *   x       bf16 [T][H]        W_r bf16 [E][H]        g bf16 [H] or NULL
+ *   logits  fp32 [T][E + (g != NULL)], fp32 accumulation of bf16 products.
+ * T = 0 is a no-op. */
+MOE_API int moe_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
+                      int T, int H, int E, float* logits, moe_stream_t stream);
+
+/* Softmax top-k router (stage 1; one warp per token, the logit row held in
+ * registers, one read of the row: vllm.cpp PR #481).
+ *   logits     fp32 (logits_is_bf16 = 0) or bf16 (= 1) [T][ld], ld >= E; only
+ *              the first E entries of a row are read
+ *   topk_ids   int32 [T][k]: the k experts with the largest logits, ties broken
+ *              towards the lower index, written in ascending expert id
+ *   topk_w     fp32  [T][k]: softmax(row)[id] / sum of softmax over the k picks
+ * A NaN logit is treated as -inf for selection.  1 <= k <= min(E, 32),
+ * E <= 256. */
+MOE_API int moe_router_topk(const void* logits, int logits_is_bf16, int ld, int T, int E,
+                    int k, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
+
+/* Dispatch (stage 2): atomic-free per-expert histogram, exclusive scan and a
+ * stable permutation of the T*k slots a = t*k + j.
+ *   counts   int32 [E] or NULL     offsets int32 [E+1] (offsets[E] = T*k)
+ *   perm     int32 [T*k]: bucket by bucket (ascending expert), the slots in
+ *            ascending order;  inv int32 [T*k]: inv[perm[r]] = r
+ * An id outside [0, E) sets MOE_ERR_DEVICE_INDEX in the workspace status word
+ * and is left out of every bucket. */
+MOE_API size_t moe_dispatch_workspace_size(int T, int k, int E);
+MOE_API int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* counts,
+                 int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
+                 size_t ws_bytes, moe_stream_t stream);
+
+/* Expert MLP (stage 3) for every dispatched row, unweighted:
+ *   rows fp32 [T*k][H]: rows[r] = W_d[e] (silu(W_g[e] x_t) * (W_u[e] x_t)) with
+ *   a = perm[r], t = a / k, e the bucket holding r (offsets[e] <= r < offsets[e+1]).
+ *   x bf16 [T][H]; offsets/perm as produced by moe_dispatch.
+ *   arm: MOE_ARM_* (which kernels compute it). */
+MOE_API size_t moe_expert_mlp_workspace_size(int T, int k, int E, int H, int I);
+MOE_API int moe_expert_mlp(const uint16_t* x, int T, int k, const moe_experts* W,
+                   const int32_t* offsets, const int32_t* perm, float* rows,
+                   int arm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Combine (stage 4): y[t] = shared[t] + sum_j topk_w[t][j] * rows[inv[t*k+j]]
+ * + residual[t], summed in that order (shared row, slots by j, residual).
+ *   rows fp32 [T*k][H] (dispatch order)   inv int32 [T*k]   topk_w fp32 [T][k]
+ *   shared fp32 [T][H] or NULL (already gated)   residual bf16 [T][H] or NULL
+ *   y fp32 [T][H] */
+MOE_API int moe_combine(const float* rows, const int32_t* inv, const float* topk_w,
+                const float* shared, const uint16_t* residual, int T, int k, int H,
+                float* y, moe_stream_t stream);
+
+/* The whole layer: logits (with the shared gate row), top-k, dispatch, expert
+ * MLP with the combine fused into the down projection, shared expert.
+ *   x bf16 [T][H]; residual bf16 [T][H] or NULL; W_r bf16 [E][H];
+ *   sh: shared expert or NULL; y fp32 [T][H];
+ *   topk_ids_out int32 [T][k] / topk_w_out fp32 [T][k]: optional copies.
+ * T = 0 is a no-op. */
+MOE_API size_t moe_workspace_size(int T, int E, int k, int H, int I, int I_sh);
+MOE_API int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r,
+                      const moe_experts* W, const moe_shared* sh, int T, int k,
+                      float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
+                      void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Clears the device status word of a workspace (its first 256 bytes) on `stream`.  Call it
+ * once on a new workspace (or allocate the workspace zero-filled) before the calls above. */
+MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronises `stream`, copies the device status word of a workspace used by
+ * the calls above into *status (MOE_OK or a MOE_ERR_DEVICE_* code) and clears
+ * it.  Returns MOE_OK, or MOE_ERR_CUDA / MOE_ERR_INVALID_ARG. */
+MOE_API int moe_device_status(void* ws, size_t ws_bytes, int* status, moe_stream_t stream);
+
+/* Measurement support (not part of the layer).
+ * moe_launch_count: number of kernels this library has launched in the process.
+ * moe_profile_enable(1): from now on every kernel launch is bracketed by a CUDA event pair on
+ *   its stream (moe_profile_enable(0) stops; both reset the totals).
+ * moe_profile_read: waits for the recorded events and returns, per kernel name, the summed
+ *   device time in ms and the number of launches.  names receives up to max_n
+ *   NUL-terminated names of name_len bytes each; *n receives the number of kernel names. */
+MOE_API long long moe_launch_count(void);
+MOE_API int moe_profile_enable(int on);
+MOE_API int moe_profile_read(int max_n, char* names, int name_len, double* ms, long* launches, int* n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,669 @@
+// gemm_sm100.cu -- tensor arm of the expert MLP (prefill batches): grouped GEMMs on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Each expert's bucket of dispatched rows is cut into tiles of up to 128 rows (daScript
+// PR #3988 "dasLLAMA vulkan: a MoE that fits the card ...", routed-block commit: the bucket
+// schedule places the buckets and their tiles; a tile with no rows returns at once).  A CTA
+// computes one (weight row block of 128, token tile) pair:
+//   A = 128 weight rows, int4 offset-binary with fp16 scales per 32 columns (colibri PR #418
+//       "Vulkan backend: expert tier + dense + MLA attention on any Vulkan 1.2 GPU",
+//       Correctness and "Grouped scales in the Vulkan kernels"), expanded by four producer
+//       warps into fp16 (nibble - 8) * scale directly in the 128-byte-swizzled K-major
+//       layout the tensor core reads;
+//   B = the tile's activation rows (fp16), brought in by TMA with the same swizzle;
+//   D = A * B^T in tensor memory (fp32), 128 lanes x N columns, N = tile rows rounded to 16.
+// Gate and up run as two accumulators of one CTA, so the epilogue forms silu(g) * u (the
+// fused gate+up+silu of colibri PR #418, Summary) and writes h in fp16.  The down GEMM's
+// epilogue writes either the unweighted rows (dispatch order), the rows weighted by their
+// top-k weight in slot order (the tensor arm's combine feed), or the shared expert's rows
+// scaled by sigmoid of its gate logit.
+//
+// Roles in a CTA of 192 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
+// memory and issues the MMAs (one thread), warps 2-5 dequantise A and then run the epilogue.
+// Every mbarrier wait is bounded; a wait that runs out records MOE_ERR_DEVICE_TIMEOUT in the
+// status word, stops the CTA's loops, drains its own copies and MMAs, frees its tensor
+// memory and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int BM = 128;           // weight rows per tile (MMA M)
+constexpr int BN = kGemmTileN;    // tokens per tile (MMA N upper bound)
+constexpr int BK = 64;            // K per pipeline stage: 128 bytes of fp16 per row
+constexpr int kTileBytesA = BM * BK * 2;
+constexpr int kTileBytesB = BN * BK * 2;
+constexpr int kStagesGU = 4;
+constexpr int kStagesDN = 6;
+constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+struct GemmK {
+    CUtensorMap tm_r;     // B operand of routed tiles
+    CUtensorMap tm_s;     // B operand of shared-expert tiles
+    int T, k, E;
+    int K_r, K_s;         // reduction length (H for gate/up, I or I_sh for down)
+    int M_r, M_s;         // weight rows (I or I_sh for gate/up, H for down)
+    int mblk_r, mblk_s;   // weight row blocks
+    int ctas_r;           // routed CTAs in the grid (ntile_max * mblk_r)
+    int out_mode;         // down: 0 rows (unweighted, dispatch order), 1 weighted slots
+    int sh_row0;          // B row of the first shared token in tm_s
+    const int* tiles;     // [2 * ntile] (expert, first dispatch row)
+    const int* n_tiles;
+    const int32_t* offsets;
+    const int32_t* perm;
+    const float* topk_w;
+    const float* sh_gate_logit;
+    int logit_ld;
+    const uint8_t* qa_r;  // gate (gate/up) or down (down) of the routed experts
+    const uint16_t* sa_r;
+    const uint8_t* qb_r;  // up (gate/up only)
+    const uint16_t* sb_r;
+    const uint8_t* qa_s;
+    const uint16_t* sa_s;
+    const uint8_t* qb_s;
+    const uint16_t* sb_s;
+    uint16_t* h_r;        // gate/up out: fp16 [T*k][M_r]
+    uint16_t* h_s;        // gate/up out: fp16 [T][M_s]
+    float* out_r;         // down out: [T*k][H]
+    float* out_s;         // down out: [T][H]
+    int* status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait: false when the CTA is aborting or the limit ran out (then it records the
+// timeout and raises the abort flag for every role of the CTA).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, int where) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 255) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                *abort_flag = 1;
+                record_status(status, MOE_ERR_DEVICE_TIMEOUT, where, static_cast<int>(blockIdx.x));
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major operand tile in the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes
+// apart, 16-byte chunk c of row r stored at chunk c ^ (r & 7).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128.
+__device__ __forceinline__ uint32_t idesc_f16_m128(int n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 8 nibbles (columns 0..7 at bits 4c) times one fp16 scale -> 8 fp16 in column order.
+__device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
+    const uint32_t t0 = (w & 0x000F000Fu) | 0x64006400u;          // cols 0, 4 as 1024 + n
+    const uint32_t t1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;   // cols 1, 5
+    const uint32_t t2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;   // cols 2, 6
+    const uint32_t t3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;  // cols 3, 7
+    const uint32_t p01 = __byte_perm(t0, t1, 0x5410);
+    const uint32_t p23 = __byte_perm(t2, t3, 0x5410);
+    const uint32_t p45 = __byte_perm(t0, t1, 0x7632);
+    const uint32_t p67 = __byte_perm(t2, t3, 0x7632);
+    const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    uint4 out;
+    __half2 v;
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p01), k1032), s2);
+    out.x = *reinterpret_cast<uint32_t*>(&v);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p23), k1032), s2);
+    out.y = *reinterpret_cast<uint32_t*>(&v);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p45), k1032), s2);
+    out.z = *reinterpret_cast<uint32_t*>(&v);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p67), k1032), s2);
+    out.w = *reinterpret_cast<uint32_t*>(&v);
+    return out;
+}
+
+struct RawK {  // one K-step of one weight row: 32 bytes of nibbles + two fp16 scales
+    uint4 q0, q1;
+    uint32_t s;
+};
+
+__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, bool valid) {
+    RawK r;
+    if (valid) {
+        const uint4* p = reinterpret_cast<const uint4*>(qrow + kb * 32);
+        r.q0 = ldg_nc(p);
+        r.q1 = ldg_nc(p + 1);
+        r.s = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 2));
+    } else {
+        r.q0 = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // all zero weights
+        r.q1 = r.q0;
+        r.s = 0;
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, const RawK& r) {
+    const __half2 s_lo = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.s & 0xffffu)));
+    const __half2 s_hi = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.s >> 16)));
+    const uint32_t w[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+    uint8_t* rowp = tile + row * 128;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint4 v = dequant8(w[m], m < 4 ? s_lo : s_hi);
+        *reinterpret_cast<uint4*>(rowp + ((m ^ (row & 7)) << 4)) = v;
+    }
+}
+
+template <int MODE>  // 0 = gate+up (two accumulators, SwiGLU epilogue), 1 = down
+__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ GemmK p) {
+    constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
+    constexpr int NMAT = MODE == 0 ? 2 : 1;
+    constexpr int kStageBytes = NMAT * kTileBytesA + kTileBytesB;
+    constexpr uint32_t kTmemCols = MODE == 0 ? 2 * BN : BN;
+
+    // ---- which tile this CTA computes
+    const bool shared = static_cast<int>(blockIdx.x) >= p.ctas_r;
+    int e, row0, nrows, mblk, K, M;
+    if (!shared) {
+        const int tix = blockIdx.x / p.mblk_r;
+        mblk = blockIdx.x % p.mblk_r;
+        if (tix >= *p.n_tiles) return;  // tile beyond the schedule: nothing to do
+        e = p.tiles[2 * tix];
+        row0 = p.tiles[2 * tix + 1];
+        nrows = min(BN, p.offsets[e + 1] - row0);
+        K = p.K_r;
+        M = p.M_r;
+    } else {
+        const int sid = blockIdx.x - p.ctas_r;
+        const int tix = sid / p.mblk_s;
+        mblk = sid % p.mblk_s;
+        e = -1;
+        row0 = tix * BN;
+        nrows = min(BN, p.T - row0);
+        K = p.K_s;
+        M = p.M_s;
+    }
+    if (nrows <= 0) return;
+    const int nk = K / BK;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    uint64_t* full_b = full_a + S;
+    uint64_t* empty = full_b + S;
+    uint64_t* accum = empty + S;
+    uint64_t* drain = accum + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_a + s, 128);
+            mbar_init(full_b + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(accum, 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto stage_a = [&](int s, int mat) { return smem + s * kStageBytes + mat * kTileBytesA; };
+    auto stage_b = [&](int s) { return smem + s * kStageBytes + NMAT * kTileBytesA; };
+
+    if (warp == 0) {
+        // ---------------- TMA producer of B
+        if (lane == 0) {
+            const CUtensorMap* tm = shared ? &p.tm_s : &p.tm_r;
+            const int brow = shared ? p.sh_row0 + row0 : row0;
+            int issued = 0;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % S;
+                if (kb >= S && !mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 1)) break;
+                mbar_arrive_expect_tx(full_b + s, kTileBytesB);
+                tma_load_2d(stage_b(s), tm, kb * BK, brow, full_b + s);
+                issued = kb + 1;
+            }
+            if (*abort_flag) {
+                // let the copies this thread started land before the CTA leaves
+                for (int kb = max(0, issued - S); kb < issued; ++kb) {
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(full_b + kb % S, (kb / S) & 1) && clock64() - t0 < kWaitLimitCycles) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            const int nmma = (nrows + 15) & ~15;
+            const uint32_t idesc = idesc_f16_m128(nmma);
+            bool any = false;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % S;
+                const uint32_t par = (kb / S) & 1;
+                if (!mbar_wait(full_b + s, par, abort_flag, p.status, 2)) break;
+                if (!mbar_wait(full_a + s, par, abort_flag, p.status, 3)) break;
+                tc_fence_after();
+                const uint32_t b0 = smem_u32(stage_b(s));
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
+                    const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+#pragma unroll
+                    for (int mat = 0; mat < NMAT; ++mat) {
+                        const uint64_t ad = sw128_kmajor_desc(smem_u32(stage_a(s, mat)) + kk * 32);
+                        mma_f16(tmem + mat * BN, ad, bd, idesc, acc);
+                    }
+                }
+                mma_commit(empty + s);
+                any = true;
+            }
+            if (!*abort_flag) {
+                mma_commit(accum);
+            } else if (any) {
+                mma_commit(drain);  // wait for this thread's MMAs before tensor memory is freed
+                const long long t0 = clock64();
+                while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+                }
+            }
+        }
+    } else {
+        // ---------------- A producers, then the epilogue (warps 2..5, 128 threads)
+        const int pr = threadIdx.x - 64;  // weight row within the block
+        const int wrow = mblk * BM + pr;  // weight row within the matrix
+        const bool valid = wrow < M;
+        const size_t grow = shared ? static_cast<size_t>(wrow) : static_cast<size_t>(e) * M + wrow;
+        const uint8_t* qa = (shared ? p.qa_s : p.qa_r) + grow * (K / 2);
+        const uint16_t* sa = (shared ? p.sa_s : p.sa_r) + grow * (K / 32);
+        const uint8_t* qb = nullptr;
+        const uint16_t* sb = nullptr;
+        if (MODE == 0) {
+            qb = (shared ? p.qb_s : p.qb_r) + grow * (K / 2);
+            sb = (shared ? p.sb_s : p.sb_r) + grow * (K / 32);
+        }
+        RawK ra = load_raw(qa, sa, 0, valid), rb{};
+        if (MODE == 0) rb = load_raw(qb, sb, 0, valid);
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            RawK na{}, nb{};
+            if (kb + 1 < nk) {
+                na = load_raw(qa, sa, kb + 1, valid);
+                if (MODE == 0) nb = load_raw(qb, sb, kb + 1, valid);
+            }
+            if (kb >= S && !mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4)) {
+                ok = false;
+                break;
+            }
+            store_dequant(stage_a(s, 0), pr, ra);
+            if (MODE == 0) store_dequant(stage_a(s, 1), pr, rb);
+            fence_proxy_async_smem();
+            mbar_arrive(full_a + s);
+            ra = na;
+            if (MODE == 0) rb = nb;
+        }
+        // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp)
+        bool go = __all_sync(0xffffffffu, ok);
+        if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5));
+        if (go) {
+            tc_fence_after();
+            const int q = warp & 3;               // tensor-memory lane quadrant of this warp
+            const int m = q * 32 + lane;          // accumulator row = weight row in the block
+            const int n_out = mblk * BM + m;      // output feature
+            const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            for (int c0 = 0; c0 < nrows; c0 += 16) {
+                float d0[16];
+                tmem_ld16(tbase + c0, d0);
+                if (MODE == 0) {
+                    float d1[16];
+                    tmem_ld16(tbase + BN + c0, d1);
+                    uint16_t* hout = shared ? p.h_s : p.h_r;
+                    if (n_out < M) {
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) {
+                            const int c = c0 + cc;
+                            if (c < nrows) {
+                                const float g = d0[cc], u = d1[cc];
+                                const float h = g / (1.f + expf(-g)) * u;
+                                hout[static_cast<size_t>(row0 + c) * M + n_out] = __half_as_ushort(__float2half_rn(h));
+                            }
+                        }
+                    }
+                } else {
+                    if (n_out < M) {
+#pragma unroll
+                        for (int cc = 0; cc < 16; ++cc) {
+                            const int c = c0 + cc;
+                            if (c >= nrows) continue;
+                            const int r = row0 + c;
+                            if (shared) {
+                                float gate = 1.f;
+                                if (p.sh_gate_logit) {
+                                    const float z = __ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld);
+                                    gate = 1.f / (1.f + expf(-z));
+                                }
+                                p.out_s[static_cast<size_t>(r) * M + n_out] = gate * d0[cc];
+                            } else if (p.out_mode == 0) {
+                                p.out_r[static_cast<size_t>(r) * M + n_out] = d0[cc];
+                            } else {
+                                const int a = __ldg(p.perm + r);
+                                p.out_r[static_cast<size_t>(a) * M + n_out] = __ldg(p.topk_w + a) * d0[cc];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ small helpers
+// Tile list from the bucket offsets: tiles of up to BN rows per expert, expert-major.
+__global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ offsets, int E,
+                                                          int* __restrict__ tiles, int* __restrict__ n_tiles) {
+    __shared__ int warp_tot[8];
+    const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+    const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
+    const int nt = (cnt + BN - 1) / BN;
+    int incl = nt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    int base = incl - nt;
+    for (int i = 0; i < w; ++i) base += warp_tot[i];
+    if (e == 255) *n_tiles = base + nt;
+    for (int j = 0; j < nt; ++j) {
+        tiles[2 * (base + j)] = e;
+        tiles[2 * (base + j) + 1] = offsets[e] + j * BN;
+    }
+}
+
+// x16[r] = fp16(x[perm[r] / k]) for the T*k dispatched rows, then x16[T*k + t] = fp16(x[t]).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
+                                                          const int32_t* __restrict__ perm, int T, int k, int H,
+                                                          int with_tokens, uint16_t* __restrict__ x16) {
+    const int n_rows = T * k + (with_tokens ? T : 0);
+    const int H8 = H / 8;
+    const long total = static_cast<long>(n_rows) * H8;
+    for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / H8), c = static_cast<int>(i % H8);
+        const int t = (r < T * k) ? __ldg(perm + r) / k : r - T * k;
+        const uint4 v = ldg_nc(x + static_cast<size_t>(t) * H + c * 8);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half lo = __float2half_rn(__uint_as_float(in[j] << 16));
+            const __half hi = __float2half_rn(__uint_as_float(in[j] & 0xffff0000u));
+            out[j] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+        }
+        reinterpret_cast<uint4*>(x16 + static_cast<size_t>(r) * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(ptr);
+    }();
+    return fn;
+}
+
+// 2D fp16 tensor [rows][K], box = 64 x BN, 128-byte swizzle, zero fill outside.
+static bool make_tmap(CUtensorMap* m, const void* base, int K, int rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {BK, BN};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_ntile_max(int n_slots, int E) { return (n_slots + BN - 1) / BN + E; }
+
+bool gemm_supported(int H, int I, int I_sh) {
+    return H % BK == 0 && I % BK == 0 && (I_sh <= 0 || I_sh % BK == 0);
+}
+
+template <int MODE>
+static size_t gemm_smem_bytes() {
+    constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
+    constexpr int NMAT = MODE == 0 ? 2 : 1;
+    return static_cast<size_t>(S) * (NMAT * kTileBytesA + kTileBytesB) + 1024 + 256;
+}
+
+template <int MODE>
+static cudaError_t set_smem_attr() {
+    static cudaError_t once = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(gemm_smem_bytes<MODE>()));
+    return once;
+}
+
+cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) {
+    cudaError_t err;
+    const int n_slots = p.T * p.k;
+    const bool has_sh = p.sh_I > 0;
+    if ((err = set_smem_attr<0>()) != cudaSuccess) return err;
+    if ((err = set_smem_attr<1>()) != cudaSuccess) return err;
+    // 1. activations in dispatch order (and token order for the shared expert), fp16
+    {
+        const long total = static_cast<long>(n_slots + (has_sh ? p.T : 0)) * (p.H / 8);
+        long blocks = (total + 255) / 256;
+        if (blocks > 152L * 8) blocks = 152L * 8;
+        if (blocks < 1) blocks = 1;
+        {
+            KernelScope ks_("gather_rows", st);
+            gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p.x, p.perm, p.T, p.k, p.H, has_sh ? 1 : 0,
+                                                                             p.x16);
+        }
+    }
+    // 2. tile schedule
+    {
+        KernelScope ks_("build_tiles", st);
+        build_tiles_kernel<<<1, 256, 0, st>>>(p.offsets, p.E, p.tiles, p.n_tiles);
+    }
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+
+    // 3. gate + up
+    GemmK g{};
+    g.T = p.T;
+    g.k = p.k;
+    g.E = p.E;
+    g.tiles = p.tiles;
+    g.n_tiles = p.n_tiles;
+    g.offsets = p.offsets;
+    g.perm = p.perm;
+    g.topk_w = p.topk_w;
+    g.sh_gate_logit = p.sh_gate_logit;
+    g.logit_ld = p.logit_ld;
+    g.status = p.status;
+    g.K_r = p.H;
+    g.K_s = p.H;
+    g.M_r = p.I;
+    g.M_s = has_sh ? p.sh_I : BM;
+    g.mblk_r = (p.I + BM - 1) / BM;
+    g.mblk_s = has_sh ? (p.sh_I + BM - 1) / BM : 1;
+    g.ctas_r = p.ntile_max * g.mblk_r;
+    g.sh_row0 = n_slots;
+    if (!make_tmap(&g.tm_r, p.x16, p.H, n_slots + (has_sh ? p.T : 0))) return cudaErrorInvalidValue;
+    g.tm_s = g.tm_r;
+    g.qa_r = p.gate_q;
+    g.sa_r = p.gate_s;
+    g.qb_r = p.up_q;
+    g.sb_r = p.up_s;
+    g.qa_s = p.sh_gate_q;
+    g.sa_s = p.sh_gate_s;
+    g.qb_s = p.sh_up_q;
+    g.sb_s = p.sh_up_s;
+    g.h_r = p.h16;
+    g.h_s = p.sh_h16;
+    {
+        const int ctas = g.ctas_r + (has_sh ? p.sh_tiles * g.mblk_s : 0);
+        {
+            KernelScope ks_("gemm_gateup", st);
+            moe_gemm_kernel<0><<<ctas, 192, gemm_smem_bytes<0>(), st>>>(g);
+        }
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    // 4. down (+ weighting / shared gate in the epilogue)
+    GemmK d = g;
+    d.K_r = p.I;
+    d.K_s = has_sh ? p.sh_I : BK;
+    d.M_r = p.H;
+    d.M_s = p.H;
+    d.mblk_r = (p.H + BM - 1) / BM;
+    d.mblk_s = d.mblk_r;
+    d.ctas_r = p.ntile_max * d.mblk_r;
+    d.sh_row0 = 0;
+    d.out_mode = rows_mode ? 0 : 1;
+    if (!make_tmap(&d.tm_r, p.h16, p.I, n_slots)) return cudaErrorInvalidValue;
+    if (has_sh) {
+        if (!make_tmap(&d.tm_s, p.sh_h16, p.sh_I, p.T)) return cudaErrorInvalidValue;
+    } else {
+        d.tm_s = d.tm_r;
+    }
+    d.qa_r = p.down_q;
+    d.sa_r = p.down_s;
+    d.qb_r = nullptr;
+    d.sb_r = nullptr;
+    d.qa_s = p.sh_down_q;
+    d.sa_s = p.sh_down_s;
+    d.qb_s = nullptr;
+    d.sb_s = nullptr;
+    d.out_r = rows_mode ? p.rows_out : p.slot_out;
+    d.out_s = p.sh_out;
+    {
+        const int ctas = d.ctas_r + (has_sh ? p.sh_tiles * d.mblk_s : 0);
+        {
+            KernelScope ks_("gemm_down", st);
+            moe_gemm_kernel<1><<<ctas, 192, gemm_smem_bytes<1>(), st>>>(d);
+        }
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

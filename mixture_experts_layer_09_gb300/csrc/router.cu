@@ -1,0 +1,281 @@
+// router.cu -- stage 1 of the routed MoE layer: router logits and the softmax top-k.
+//
+// Logits: one dot product per (token, router row) in fp32 over bf16 products, with the
+// shared-expert gate vector as one more row past the router's E rows (daScript PR #3988
+// "dasLLAMA vulkan: a MoE that fits the card ...", decode span commit: the gate logit is one
+// more router GEMV row).  Decode batches (T <= 32) run a GEMV that reads every router row
+// once; larger batches run a tiled fp32 GEMM.
+//
+// Top-k: one warp per token with the whole logit row in registers, no shared memory, no
+// block barrier and one read of the row (vllm.cpp PR #481 "gate(#378): the first DEVICE run
+// of the warp MoE router", warp-router commit).  Selection is k rounds of a warp argmax with
+// the lowest index winning a tie; weights are the fp32 softmax over all E logits renormalised
+// over the k picks; the picks are written in ascending expert id.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ logits, decode GEMV
+// One CTA (128 threads) per router row; thread c covers 16-byte chunks c, c+128, ... of H.
+template <int TB>
+__global__ void __launch_bounds__(128) router_logits_gemv_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
+    int T, int H, int E, int ld, float* __restrict__ logits) {
+    const int row = blockIdx.x;  // 0..E-1 router rows, E = gate row
+    const uint16_t* w = (row < E) ? W_r + static_cast<size_t>(row) * H : g;
+    const int nch = H / 8;
+    __shared__ float red[4][TB];
+    for (int t0 = 0; t0 < T; t0 += TB) {
+        float acc[TB];
+#pragma unroll
+        for (int i = 0; i < TB; ++i) acc[i] = 0.f;
+        for (int c = threadIdx.x; c < nch; c += 128) {
+            uint4 wv = ldg_nc(w + static_cast<size_t>(c) * 8);
+            float wf[8];
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                wf[2 * q] = __uint_as_float(ww[q] << 16);
+                wf[2 * q + 1] = __uint_as_float(ww[q] & 0xffff0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < TB; ++i) {
+                if (t0 + i < T) {
+                    uint4 xv = ldg_nc(x + static_cast<size_t>(t0 + i) * H + static_cast<size_t>(c) * 8);
+                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[i] = fmaf(__uint_as_float(xx[q] << 16), wf[2 * q], acc[i]);
+                        acc[i] = fmaf(__uint_as_float(xx[q] & 0xffff0000u), wf[2 * q + 1], acc[i]);
+                    }
+                }
+            }
+        }
+        const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+        for (int i = 0; i < TB; ++i) {
+            float v = warp_sum(acc[i]);
+            if (lane == 0) red[wid][i] = v;
+        }
+        __syncthreads();
+        if (threadIdx.x < TB && t0 + threadIdx.x < T) {
+            const int i = threadIdx.x;
+            logits[static_cast<size_t>(t0 + i) * ld + row] = (red[0][i] + red[1][i]) + (red[2][i] + red[3][i]);
+        }
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ logits, prefill GEMM
+// Tile: 64 tokens x 32 router rows, K step 32; 256 threads, each 4 tokens x 2 rows.
+constexpr int RG_BT = 64, RG_BR = 32, RG_BK = 32;
+
+__global__ void __launch_bounds__(256) router_logits_gemm_kernel(
+    const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
+    int T, int H, int E, int nrows, int ld, float* __restrict__ logits) {
+    __shared__ float xs[RG_BK][RG_BT + 4];
+    __shared__ float ws[RG_BK][RG_BR + 4];
+    const int t0 = blockIdx.x * RG_BT, r0 = blockIdx.y * RG_BR;
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // tx: rows (2 each), ty: tokens (4 each)
+    float acc[4][2] = {};
+    for (int k0 = 0; k0 < H; k0 += RG_BK) {
+        // x tile: 64 tokens x 32 k = 2048 values, 8 per thread (one 16-byte load)
+        {
+            const int tt = threadIdx.x >> 2, kk = (threadIdx.x & 3) * 8;
+            const int t = t0 + tt;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t < T) v = ldg_nc(x + static_cast<size_t>(t) * H + k0 + kk);
+            const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                xs[kk + 2 * q][tt] = __uint_as_float(vv[q] << 16);
+                xs[kk + 2 * q + 1][tt] = __uint_as_float(vv[q] & 0xffff0000u);
+            }
+        }
+        // router tile: 32 rows x 32 k = 1024 values, 4 per thread
+        {
+            const int rr = threadIdx.x >> 3, kk = (threadIdx.x & 7) * 4;
+            const int r = r0 + rr;
+            uint2 v = make_uint2(0, 0);
+            if (r < nrows) {
+                const uint16_t* src = (r < E) ? W_r + static_cast<size_t>(r) * H : g;
+                v = *reinterpret_cast<const uint2*>(src + k0 + kk);
+            }
+            ws[kk + 0][rr] = __uint_as_float(v.x << 16);
+            ws[kk + 1][rr] = __uint_as_float(v.x & 0xffff0000u);
+            ws[kk + 2][rr] = __uint_as_float(v.y << 16);
+            ws[kk + 3][rr] = __uint_as_float(v.y & 0xffff0000u);
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < RG_BK; ++kk) {
+            float xv[4], wv[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = xs[kk][ty * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) wv[j] = ws[kk][tx * 2 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int t = t0 + ty * 4 + i;
+        if (t >= T) continue;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int r = r0 + tx * 2 + j;
+            if (r < nrows) logits[static_cast<size_t>(t) * ld + r] = acc[i][j];
+        }
+    }
+}
+
+cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
+                                 int E, float* logits, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int nrows = E + (g ? 1 : 0);
+    const int ld = nrows;
+    if (T <= 32) {
+        KernelScope ks_("router_logits_gemv", st);
+        if (T <= 4)
+            router_logits_gemv_kernel<4><<<nrows, 128, 0, st>>>(x, W_r, g, T, H, E, ld, logits);
+        else
+            router_logits_gemv_kernel<8><<<nrows, 128, 0, st>>>(x, W_r, g, T, H, E, ld, logits);
+    } else {
+        KernelScope ks_("router_logits_gemm", st);
+        const dim3 grid((T + RG_BT - 1) / RG_BT, (nrows + RG_BR - 1) / RG_BR);
+        router_logits_gemm_kernel<<<grid, 256, 0, st>>>(x, W_r, g, T, H, E, nrows, ld, logits);
+    }
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ softmax top-k
+template <typename Tin>
+__device__ __forceinline__ float load_logit(const Tin* p);
+template <>
+__device__ __forceinline__ float load_logit<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p) { return bf16_to_f32(__ldg(p)); }
+
+// VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
+template <typename Tin, int VPT>
+__global__ void __launch_bounds__(256) router_topk_warp_kernel(
+    const Tin* __restrict__ logits, int ld, int T, int E, int k,
+    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const Tin* row = logits + static_cast<size_t>(t) * ld;
+    float v[VPT];
+    bool picked[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E) {
+            float f = load_logit<Tin>(row + e);
+            v[j] = (f != f) ? -INFINITY : f;  // NaN never wins a pick
+            picked[j] = false;
+        } else {
+            v[j] = -INFINITY;
+            picked[j] = true;  // padding is never a candidate
+        }
+    }
+    // k rounds of a warp argmax: larger value first, lower expert index on a tie.
+    for (int round = 0; round < k; ++round) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int e = lane + 32 * j;
+            if (!picked[j] && (v[j] > bv || (v[j] == bv && e < bi))) {
+                bv = v[j];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi != 0x7fffffff && (bi & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+                if (bi == lane + 32 * j) picked[j] = true;
+        }
+    }
+    // softmax over all E logits in fp32, renormalised over the picks
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+        if (lane + 32 * j < E) m = fmaxf(m, v[j]);
+    m = warp_max(m);
+    float p[VPT];
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        p[j] = (lane + 32 * j < E && m > -INFINITY) ? expf(v[j] - m) : 0.f;
+        z += p[j];
+    }
+    z = warp_sum(z);
+    float psel = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        p[j] = (z > 0.f) ? p[j] / z : 0.f;
+        if (picked[j] && lane + 32 * j < E) psel += p[j];
+    }
+    psel = warp_sum(psel);
+    // write the picks in ascending expert id: (j, lane) order
+    int base = 0;
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const bool mine = picked[j] && (lane + 32 * j < E);
+        const unsigned b = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+            const int pos = base + __popc(b & lt);
+            if (pos < k) {
+                topk_ids[static_cast<size_t>(t) * k + pos] = lane + 32 * j;
+                // denominator guard: a row with no finite logit spreads the weight evenly
+                topk_w[static_cast<size_t>(t) * k + pos] = (psel > 0.f) ? p[j] / psel : 1.f / k;
+            }
+        }
+        base += __popc(b);
+    }
+}
+
+template <typename Tin>
+static cudaError_t launch_topk_t(const Tin* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
+                                 cudaStream_t st) {
+    const int vpt = (E + 31) / 32;
+    const dim3 grid((T + 7) / 8), block(256);
+    KernelScope ks_("router_topk", st);
+    switch (vpt) {
+        case 1: router_topk_warp_kernel<Tin, 1><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 2: router_topk_warp_kernel<Tin, 2><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 3: router_topk_warp_kernel<Tin, 3><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 4: router_topk_warp_kernel<Tin, 4><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 5: router_topk_warp_kernel<Tin, 5><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 6: router_topk_warp_kernel<Tin, 6><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 7: router_topk_warp_kernel<Tin, 7><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        case 8: router_topk_warp_kernel<Tin, 8><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
+                               float* w, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    if (is_bf16) return launch_topk_t(static_cast<const uint16_t*>(logits), ld, T, E, k, ids, w, st);
+    return launch_topk_t(static_cast<const float*>(logits), ld, T, E, k, ids, w, st);
+}
+
+}  // namespace moe

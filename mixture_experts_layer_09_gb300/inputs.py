@@ -79,7 +79,10 @@ def draw_q4(seed: int, tag: int, n_mat: int, rows: int, K: int) -> Q4:
     if K % SCALE_GROUP:
         raise ValueError("K must be a multiple of 32")
     g = rng(seed, tag)
-    q = g.integers(0, 256, size=(n_mat, rows, K // 2), dtype=np.uint8)
+    nbytes = n_mat * rows * (K // 2)
+    # raw 64-bit outputs of the stream: every bit uniform, so every nibble is uniform in 0..15
+    raw = g.bit_generator.random_raw((nbytes + 7) // 8).view(np.uint8)
+    q = raw[:nbytes].reshape(n_mat, rows, K // 2).copy()
     s = f16_bits(np.abs(g.normal(0.0, 0.01, size=(n_mat, rows, K // SCALE_GROUP))) + 1e-3)
     return Q4(q, s)
 

@@ -1,0 +1,135 @@
+"""GPU parity of the expert MLP (both arms), the combine and the whole layer against the fp64
+oracle, on the workloads' shapes.  Routing (ids) is bit-exact; float outputs meet rel-L2 <= 1e-3
+and max-abs <= 2e-3 * max|ref|.  Large workloads are checked on sampled tokens, which the oracle
+computes one by one; routing is compared for every token."""
+import numpy as np
+import pytest
+
+import oracle
+from mixture_experts_layer_09_gb300 import inputs as gen
+from tests import workloads as wk
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import torch
+    import mixture_experts_layer_09_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    m.build()
+    return m
+
+
+def _routing(inp):
+    logits = oracle.router_logits(inp.x, inp.W_r).astype(np.float32).astype(np.float64)
+    ids, w = oracle.router_topk(logits, inp.wl.k)
+    return ids, w, oracle.dispatch(ids, inp.wl.E)
+
+
+@pytest.mark.parametrize("arm", [1, 2])
+@pytest.mark.parametrize("shape", [dict(T=4, H=256, I=128, E=8, k=2), dict(T=37, H=512, I=256, E=16, k=4),
+                                   dict(T=200, H=256, I=192, E=8, k=2), dict(T=3, H=2048, I=768, E=128, k=8)])
+def test_expert_mlp_rows(moe, arm, shape):
+    import torch
+    wl = gen.Workload("mlp", shape["T"], shape["H"], shape["I"], shape["E"], shape["k"], seed=11)
+    inp = wk.enforce_margin_x(gen.draw_layer(wl))
+    ids, w, (counts, offsets, perm, inv) = _routing(inp)
+    ref = oracle.expert_mlp(inp.x, inp.experts, ids, perm)
+    x, r, W_r, E, S = wk.upload(inp)
+    T, k = wl.T, wl.k
+    rows = wk.poison(torch.empty((T * k, wl.H), dtype=torch.float32, device="cuda"))
+    ws = torch.zeros(moe.moe_expert_mlp_workspace_size(T, k, wl.E, wl.H, wl.I), dtype=torch.uint8, device="cuda")
+    moe.moe_expert_mlp(x, k, E, wk.dev(offsets), wk.dev(perm), rows, ws, arm=arm)
+    assert moe.moe_device_status(ws) == 0
+    wk.assert_close(rows.cpu().numpy(), ref, f"rows arm={arm}")
+
+
+def test_combine(moe):
+    import torch
+    T, k, H = 33, 4, 256
+    g = gen.rng(12)
+    rows = g.normal(size=(T * k, H)).astype(np.float32)
+    perm = g.permutation(T * k).astype(np.int32)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(T * k, dtype=np.int32)
+    w = g.random(size=(T, k)).astype(np.float32)
+    sh = g.normal(size=(T, H)).astype(np.float32)
+    r = gen.bf16_bits(g.normal(size=(T, H)))
+    ref = oracle.combine(rows.astype(np.float64), inv, w.astype(np.float64), sh.astype(np.float64), r)
+    y = wk.poison(torch.empty((T, H), dtype=torch.float32, device="cuda"))
+    moe.moe_combine(wk.dev(rows), wk.dev(inv), wk.dev(w), wk.dev(sh), wk.dev(r.view(np.int16), torch.bfloat16), y)
+    torch.cuda.synchronize()
+    wk.assert_close(y.cpu().numpy(), ref, "combine", rel_l2_tol=1e-6)
+    ref2 = oracle.combine(rows.astype(np.float64), inv, w.astype(np.float64))
+    moe.moe_combine(wk.dev(rows), wk.dev(inv), wk.dev(w), None, None, y)
+    torch.cuda.synchronize()
+    wk.assert_close(y.cpu().numpy(), ref2, "combine (no shared, no residual)", rel_l2_tol=1e-6)
+
+
+def _layer_gpu(moe, inp, arm=0):
+    import torch
+    x, r, W_r, E, S = wk.upload(inp)
+    wl = inp.wl
+    I_sh = S.I_sh if S is not None else 0
+    ws = torch.zeros(moe.moe_workspace_size(wl.T, wl.E, wl.k, wl.H, wl.I, I_sh), dtype=torch.uint8, device="cuda")
+    y = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda"))
+    ids = wk.poison(torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda"))
+    w = wk.poison(torch.empty((wl.T, wl.k), dtype=torch.float32, device="cuda"))
+    moe.moe_layer_forward(x, r, W_r, E, S, wl.k, y, ws, ids, w, arm=arm)
+    st = moe.moe_device_status(ws)
+    return y.cpu().numpy(), ids.cpu().numpy(), w.cpu().numpy(), st
+
+
+def _check_layer(moe, inp, arm=0, sample=None):
+    T = inp.wl.T
+    if sample is None:
+        mask = None
+        toks = np.arange(T)
+    else:
+        g = gen.rng(99, T)
+        toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(sample, T), replace=False)]))
+        mask = np.zeros(T, dtype=np.uint8)
+        mask[toks] = 1
+    ref = oracle.layer_forward(inp, token_mask=mask)
+    y, ids, w, st = _layer_gpu(moe, inp, arm)
+    assert st == 0
+    assert np.array_equal(ids, ref["ids"]), "routing differs"
+    wk.assert_close(w, ref["w"], "topk_w")
+    wk.assert_close(y[toks], ref["y"][toks], f"y arm={arm}")
+
+
+@pytest.mark.parametrize("arm", [1, 2])
+@pytest.mark.parametrize("shared", [False, True])
+def test_layer_tiny(moe, arm, shared):
+    inp = wk.layer("tiny", I_sh=128 if shared else 0)
+    _check_layer(moe, inp, arm)
+
+
+def test_layer_tiny_ungated_shared_no_residual(moe):
+    inp = wk.layer("tiny", I_sh=64, gated_shared=False, residual=False, T=40)
+    _check_layer(moe, inp, 1)
+    _check_layer(moe, inp, 2)
+
+
+@pytest.mark.parametrize("name", ["qwen3_30b_decode_t1", "qwen3_30b_decode_t4", "qwen3_30b_decode_t16"])
+def test_layer_qwen3_decode(moe, name):
+    _check_layer(moe, wk.layer(name))
+
+
+@pytest.mark.parametrize("name,sample", [("glm_decode_k8_t1", None), ("glm_decode_k8_t8", 3),
+                                         ("glm_decode_k32_t1", None), ("glm_decode_k32_t8", 2)])
+def test_layer_glm_decode(moe, name, sample):
+    _check_layer(moe, wk.layer(name), sample=sample)
+
+
+@pytest.mark.parametrize("name,sample", [("qwen15_prefill_t512", 6), ("qwen15_prefill_t4096", 6)])
+def test_layer_qwen15_prefill(moe, name, sample):
+    _check_layer(moe, wk.layer(name), sample=sample)
+
+
+def test_layer_qwen15_prefill_gemv_arm_agrees(moe):
+    """Both arms on the same prefill batch: each within tolerance of the oracle."""
+    inp = wk.layer("qwen15_prefill_t512", T=96)
+    _check_layer(moe, inp, arm=1, sample=4)
+    _check_layer(moe, inp, arm=2, sample=4)
