@@ -140,6 +140,26 @@ MOE_API int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* 
                  int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
                  size_t ws_bytes, moe_stream_t stream);
 
+/* moe_dispatch without a workspace (the pages have no counterpart: this entry point
+ * exists for callers, not for the method).  Some callers cannot allocate device memory
+ * when they dispatch: a host framework whose device memory pool is fixed at start-up, a
+ * serving runtime's plugin callback that is not allowed to allocate, or a latency-bound
+ * loop that cannot afford the device synchronisation an allocation implies.  This variant
+ * runs the same kernels as moe_dispatch with their scratch in one array compiled into the
+ * library (about 514 KiB, held on every GPU that loads the library until the process
+ * exits), and allocates nothing.
+ *   Arguments and outputs are those of moe_dispatch; T*k must not exceed
+ *   MOE_DISPATCH_STATIC_MAX_SLOTS (else MOE_ERR_INVALID_ARG, nothing enqueued).
+ *   The first call on a device looks up the array's device address (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   Every call on a device shares the one array and each call clears its status word first:
+ *   calls that overlap on the GPU (other streams, other host threads) race and must be
+ *   serialised by the caller.  An id outside [0, E) is left out of every bucket (its inv
+ *   entry is -1); there is no status word to read back. */
+#define MOE_DISPATCH_STATIC_MAX_SLOTS (1 << 20)
+MOE_API int moe_dispatch_static(const int32_t* topk_ids, int T, int k, int E, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* inv, moe_stream_t stream);
+
 /* Expert MLP (stage 3) for every dispatched row, unweighted:
  *   rows fp32 [T*k][H]: rows[r] = W_d[e] (silu(W_g[e] x_t) * (W_u[e] x_t)) with
  *   a = perm[r], t = a / k, e the bucket holding r (offsets[e] <= r < offsets[e+1]).

@@ -60,6 +60,7 @@ _SIGS = {
     "moe_router_topk": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "moe_dispatch_workspace_size": (_S, [_I, _I, _I]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_dispatch_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_mlp_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "moe_expert_mlp": (_I, [_P, _I, _I, C.POINTER(moe_experts), _P, _P, _P, _I, _P, _S, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _P, _P]),
@@ -205,6 +206,18 @@ def moe_dispatch(topk_ids, E: int, counts, offsets, perm, inv, ws, stream=None):
         _need(t, 4, w)
     _check(lib().moe_dispatch(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
                               _ptr(ws), ws.numel(), _stream(stream)), "moe_dispatch")
+    return counts, offsets, perm, inv
+
+
+def moe_dispatch_static(topk_ids, E: int, counts, offsets, perm, inv, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate device memory at call
+    time; scratch lives in a fixed array inside the library, shared by every call on a device
+    (overlapping calls race).  T*k is limited to 2**20."""
+    T, k = topk_ids.shape
+    for t, w in ((topk_ids, "topk_ids"), (counts, "counts"), (offsets, "offsets"), (perm, "perm"), (inv, "inv")):
+        _need(t, 4, w)
+    _check(lib().moe_dispatch_static(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm), _ptr(inv),
+                                     _stream(stream)), "moe_dispatch_static")
     return counts, offsets, perm, inv
 
 

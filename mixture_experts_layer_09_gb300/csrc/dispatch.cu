@@ -222,3 +222,74 @@ cudaError_t launch_dispatch(const int32_t* ids, int n, int E, int32_t* counts, i
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------ allocation-free variant
+// moe_dispatch_static: the same three dispatch kernels, with their scratch (status word,
+// active-expert list, per-CTA count table) in one fixed array compiled into the library
+// instead of a caller workspace.  It serves callers that must not allocate device memory at
+// call time: code running under a framework whose device pool is fixed at start-up, plugin
+// callbacks of a serving runtime that forbid allocation, or latency-critical loops where an
+// allocation's implicit device synchronisation cannot be paid.  Every GPU that loads the
+// library holds the array (about 514 KiB) until the process exits.
+#include <mutex>
+
+namespace moe {
+namespace {
+constexpr size_t kStaticStatusBytes = 256;
+constexpr size_t kStaticActiveBytes = 2048;  // active list: E + 1 <= 257 ints
+constexpr size_t kStaticTableBytes =
+    static_cast<size_t>((MOE_DISPATCH_STATIC_MAX_SLOTS + kBigSlotsPerCta - 1) / kBigSlotsPerCta) * MOE_MAX_E *
+    sizeof(int);
+constexpr size_t kStaticBytes = kStaticStatusBytes + kStaticActiveBytes + kStaticTableBytes;
+}  // namespace
+}  // namespace moe
+
+static __device__ __align__(256) unsigned char g_dispatch_scratch[moe::kStaticBytes];
+
+namespace {
+constexpr int kMaxDevices = 128;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device.  The name is only a host-side
+// stand-in for the array, so the address is looked up once per device (with that device
+// current) and cached.
+int static_scratch_address(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_static_addr[dev] = p;
+    }
+    *out = g_static_addr[dev];
+    return MOE_OK;
+}
+}  // namespace
+
+extern "C" MOE_API int moe_dispatch_static(const int32_t* topk_ids, int T, int k, int E, int32_t* counts,
+                                           int32_t* offsets, int32_t* perm, int32_t* inv, moe_stream_t stream) {
+    if (T < 0 || k < 1 || k > MOE_MAX_K || E < 1 || E > MOE_MAX_E) return MOE_ERR_INVALID_ARG;
+    if (static_cast<long long>(T) * k > MOE_DISPATCH_STATIC_MAX_SLOTS) return MOE_ERR_INVALID_ARG;
+    if (!offsets || (T > 0 && (!topk_ids || !perm || !inv))) return MOE_ERR_INVALID_ARG;
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
+    void* base = nullptr;
+    if (int s = static_scratch_address(&base)) return s;
+    char* p = static_cast<char*>(base);
+    int* status = reinterpret_cast<int*>(p);
+    int32_t* active = reinterpret_cast<int32_t*>(p + moe::kStaticStatusBytes);
+    void* table = p + moe::kStaticStatusBytes + moe::kStaticActiveBytes;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the kernels record a fault only into a zero status word: clear the previous call's
+    if (cudaMemsetAsync(status, 0, moe::kStaticStatusBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return moe::launch_dispatch(topk_ids, T * k, E, counts, offsets, perm, inv, active, active + E, table, status,
+                                st) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
+}
