@@ -75,7 +75,7 @@ enum {
 };
 
 enum {
-    MOE_ARM_AUTO = 0,  /* GEMV when T <= 32, grouped GEMM otherwise */
+    MOE_ARM_AUTO = 0,  /* GEMV when T <= MOE_AUTO_GEMV_MAX_T, grouped GEMM otherwise */
     MOE_ARM_GEMV = 1,  /* bandwidth arm: fused int4 GEMV, weights streamed once per call */
     MOE_ARM_GEMM = 2   /* tensor arm: grouped GEMM on tcgen05 / TMEM */
 };
@@ -83,7 +83,8 @@ enum {
 /* Size limits checked on the host. */
 #define MOE_MAX_E 256
 #define MOE_MAX_K 32
-#define MOE_MAX_T_GEMV_COMBINE 32
+#define MOE_AUTO_GEMV_MAX_T 32
+#define MOE_MAX_H 24576
 
 typedef struct {
     const uint8_t* q;   /* device, uint8 [n_mat][rows][K/2] */
@@ -91,7 +92,7 @@ typedef struct {
 } moe_q4;
 
 typedef struct {
-    int E, H, I;        /* 1 <= E <= 256; H, I positive multiples of 32 */
+    int E, H, I;        /* 1 <= E <= 256; H, I positive multiples of 32; H <= 24576 */
     moe_q4 gate, up, down;
 } moe_experts;
 
@@ -191,8 +192,10 @@ MOE_API int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const
                       float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Clears the device status word of a workspace (its first 256 bytes) on `stream`.  Call it
- * once on a new workspace (or allocate the workspace zero-filled) before the calls above. */
+/* Clears the head of a workspace (its first 4096 bytes: the device status word and the
+ * down projection's column counters) on `stream`.  A workspace must start with a zero head:
+ * call this once on a new workspace, or allocate it zero-filled.  The calls above leave the
+ * head zero again (except a recorded status). */
 MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, copies the device status word of a workspace used by

@@ -22,7 +22,7 @@ from typing import Optional
 from . import _build
 
 ARM_AUTO, ARM_GEMV, ARM_GEMM = 0, 1, 2
-MAX_T_GEMV_COMBINE = 32
+AUTO_GEMV_MAX_T = 32
 
 _lib = None
 
@@ -166,7 +166,7 @@ class Shared:
 
 def _workspace(nbytes: int, device):
     import torch
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    return torch.zeros(max(int(nbytes), 4096), dtype=torch.uint8, device=device)
 
 
 # ----------------------------------------------------------------------------- entry points

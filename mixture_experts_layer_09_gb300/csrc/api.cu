@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "quant.cuh"
 
 using namespace moe;
 
@@ -16,7 +17,7 @@ namespace {
 // Carves 256-byte-aligned pieces out of a workspace; with base == nullptr it only measures.
 struct Carver {
     char* base;
-    size_t off = kWsAlign;  // the first 256 bytes hold the device status word
+    size_t off = kWsHead;  // status word and column counters
     explicit Carver(void* b) : base(static_cast<char*>(b)) {}
     template <typename T>
     T* take(size_t count) {
@@ -41,11 +42,10 @@ struct Routing {
 };
 
 struct GemvBufs {
-    int16_t* xq; float* xsc; int* xsum;
-    float* h; float* sh_h;
-    int16_t* hq; float* hsc; int* hsum;
-    int16_t* sh_hq; float* sh_hsc; int* sh_hsum;
-    float* rows; float* sh_rows;
+    int16_t* xq; int2* xmeta;
+    int16_t* hq; int2* hmeta;
+    int16_t* sh_hq; int2* sh_hmeta;
+    float* rows; float* sh_rows;      // ROWS mode (unweighted) / COMBINE mode (weighted slot terms)
 };
 
 struct GemmBufs {
@@ -68,23 +68,18 @@ void carve_routing(Carver& c, int T, int E, int k, Routing& r) {
     r.disp_scratch = c.take<char>(dispatch_scratch_bytes(static_cast<int>(n), E));
 }
 
-void carve_gemv(Carver& c, int T, int k, int H, int I, int I_sh, bool rows_mode, GemvBufs& b) {
+void carve_gemv(Carver& c, int T, int k, int H, int I, int I_sh, GemvBufs& b) {
     const size_t R = static_cast<size_t>(T) * k;
-    b.xq = c.take<int16_t>(static_cast<size_t>(T) * H);
-    b.xsc = c.take<float>(static_cast<size_t>(T) * (H / 32));
-    b.xsum = c.take<int>(static_cast<size_t>(T) * (H / 32));
-    b.h = c.take<float>(R * I);
-    b.hq = c.take<int16_t>(R * I);
-    b.hsc = c.take<float>(R * (I / 32));
-    b.hsum = c.take<int>(R * (I / 32));
+    b.xq = c.take<int16_t>(static_cast<size_t>(T) * act_row(H));
+    b.xmeta = c.take<int2>(static_cast<size_t>(T) * act_gld(H));
+    b.hq = c.take<int16_t>(R * act_row(I));
+    b.hmeta = c.take<int2>(R * act_gld(I));
     const size_t Ts = I_sh > 0 ? static_cast<size_t>(T) : 0;
     const int Is = I_sh > 0 ? I_sh : 32;
-    b.sh_h = c.take<float>(Ts * Is);
-    b.sh_hq = c.take<int16_t>(Ts * Is);
-    b.sh_hsc = c.take<float>(Ts * (Is / 32));
-    b.sh_hsum = c.take<int>(Ts * (Is / 32));
-    b.rows = rows_mode ? c.take<float>(R * H) : nullptr;
-    b.sh_rows = (rows_mode && I_sh > 0) ? c.take<float>(static_cast<size_t>(T) * H) : nullptr;
+    b.sh_hq = c.take<int16_t>(Ts * act_row(Is));
+    b.sh_hmeta = c.take<int2>(Ts * act_gld(Is));
+    b.rows = c.take<float>(R * H);
+    b.sh_rows = c.take<float>(Ts * H);
 }
 
 void carve_gemm(Carver& c, int T, int k, int E, int H, int I, int I_sh, GemmBufs& b) {
@@ -102,13 +97,6 @@ void carve_gemm(Carver& c, int T, int k, int E, int H, int I, int I_sh, GemmBufs
 int status_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-int num_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
 
 // The library runs only on compute capability 10.3 (sm_103a).
 int check_device() {
@@ -129,6 +117,7 @@ int check_q4(const moe_q4& m) {
 int check_experts(const moe_experts* W) {
     if (!W) return MOE_ERR_INVALID_ARG;
     if (W->E < 1 || W->E > MOE_MAX_E || W->H < 32 || W->I < 32 || W->H % 32 || W->I % 32) return MOE_ERR_INVALID_ARG;
+    if (W->H > MOE_MAX_H) return MOE_ERR_INVALID_ARG;
     int s;
     if ((s = check_q4(W->gate)) || (s = check_q4(W->up)) || (s = check_q4(W->down))) return s;
     return MOE_OK;
@@ -144,14 +133,12 @@ int check_shared(const moe_shared* sh) {
 }
 
 int choose_arm(int arm, int T, int H, int I, int I_sh) {
-    const bool gemv_ok = gemv_supported(H, I, I_sh);
     const bool gemm_ok = gemm_supported(H, I, I_sh);
-    if (arm == MOE_ARM_GEMV) return gemv_ok ? MOE_ARM_GEMV : -1;
+    if (arm == MOE_ARM_GEMV) return MOE_ARM_GEMV;
     if (arm == MOE_ARM_GEMM) return gemm_ok ? MOE_ARM_GEMM : -1;
     if (arm != MOE_ARM_AUTO) return -1;
-    if (T <= MOE_MAX_T_GEMV_COMBINE && gemv_ok) return MOE_ARM_GEMV;
-    if (gemm_ok) return MOE_ARM_GEMM;
-    return gemv_ok ? MOE_ARM_GEMV : -1;
+    if (T <= MOE_AUTO_GEMV_MAX_T || !gemm_ok) return MOE_ARM_GEMV;
+    return MOE_ARM_GEMM;
 }
 
 cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
@@ -160,6 +147,8 @@ cudaStream_t S(moe_stream_t s) { return static_cast<cudaStream_t>(s); }
 // dispatch may come from elsewhere).
 __global__ void active_from_offsets_kernel(const int32_t* __restrict__ offsets, int E, int32_t* active,
                                            int32_t* n_active) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_tot[8];
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
     const int f = (e < E && offsets[e + 1] > offsets[e]) ? 1 : 0;
@@ -197,12 +186,15 @@ struct MlpCall {
     int* status;
 };
 
-int run_gemv(const MlpCall& c, GemvBufs& b, bool fused_combine, cudaStream_t st) {
+int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
     const moe_experts* W = c.W;
     const int I_sh = c.sh ? c.sh->I_sh : 0;
-    QuantArgs qx;
-    qx.src0 = c.x; qx.src0_bf16 = 1; qx.rows0 = c.T; qx.K0 = W->H; qx.q0 = b.xq; qx.sc0 = b.xsc; qx.sum0 = b.xsum;
-    if ((launch_quantize(qx, st)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!x_quantized) {
+        QuantArgs qx;
+        qx.src0 = c.x; qx.src0_bf16 = 1; qx.rows0 = c.T; qx.K0 = W->H; qx.q0 = b.xq; qx.meta0 = b.xmeta;
+        qx.gld0 = act_gld(W->H);
+        if (launch_quantize(qx, st) != cudaSuccess) return MOE_ERR_CUDA;
+    }
     GemvArgs p{};
     p.T = c.T; p.k = c.k; p.H = W->H; p.I = W->I;
     p.max_active = std::min(W->E, c.T * c.k);
@@ -216,31 +208,23 @@ int run_gemv(const MlpCall& c, GemvBufs& b, bool fused_combine, cudaStream_t st)
         p.logit_ld = c.logit_ld;
     }
     p.offsets = c.offsets; p.perm = c.perm; p.active = c.active; p.n_active = c.n_active; p.topk_w = c.topk_w;
-    p.xq = b.xq; p.xsc = b.xsc; p.xsum = b.xsum; p.h = b.h; p.sh_h = b.sh_h;
-    p.hq = b.hq; p.hsc = b.hsc; p.hsum = b.hsum; p.sh_hq = b.sh_hq; p.sh_hsc = b.sh_hsc; p.sh_hsum = b.sh_hsum;
-    if ((launch_gateup_gemv(p, num_sms(), st)) != cudaSuccess) return MOE_ERR_CUDA;
-    QuantArgs qh;
-    qh.src0 = b.h; qh.src0_bf16 = 0; qh.rows0 = c.T * c.k; qh.K0 = W->I; qh.q0 = b.hq; qh.sc0 = b.hsc; qh.sum0 = b.hsum;
-    if (I_sh > 0) {
-        qh.src1 = b.sh_h; qh.src1_bf16 = 0; qh.rows1 = c.T; qh.K1 = I_sh; qh.q1 = b.sh_hq; qh.sc1 = b.sh_hsc;
-        qh.sum1 = b.sh_hsum;
+    p.status = c.status;
+    p.x_gld = act_gld(W->H); p.h_gld = act_gld(W->I); p.sh_gld = act_gld(I_sh > 0 ? I_sh : 32);
+    p.xq = b.xq; p.xmeta = b.xmeta;
+    p.hq = b.hq; p.hmeta = b.hmeta; p.sh_hq = b.sh_hq; p.sh_hmeta = b.sh_hmeta;
+    if (!gemv_tensor_maps(p, W->E)) return MOE_ERR_CUDA;
+    if (launch_gateup_gemv(p, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (c.rows_out) {  // stage call: unweighted rows in dispatch order
+        p.rows_out = c.rows_out;
+        p.sh_rows_out = b.sh_rows;
+        return launch_down_gemv(p, false, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
     }
-    if ((launch_quantize(qh, st)) != cudaSuccess) return MOE_ERR_CUDA;
-    if (fused_combine) {
-        p.residual = c.residual;
-        p.y = c.y;
-        if ((launch_down_gemv(p, true, st)) != cudaSuccess) return MOE_ERR_CUDA;
-        return MOE_OK;
-    }
-    p.rows_out = c.rows_out ? c.rows_out : b.rows;
-    p.sh_rows_out = b.sh_rows;
-    if ((launch_down_gemv(p, false, st)) != cudaSuccess) return MOE_ERR_CUDA;
-    if (!c.rows_out) {  // layer with T above the fused-combine limit: combine separately
-        if ((launch_combine(b.rows, c.inv, c.topk_w, false, b.sh_rows, c.residual, c.T, c.k, W->H, c.y, st)) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
-    return MOE_OK;
+    p.slot_term = b.rows;
+    p.sh_term = b.sh_rows;
+    p.col_counter = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + kWsCounterOffset);
+    p.residual = c.residual;
+    p.y = c.y;
+    return launch_down_gemv(p, true, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st) {
@@ -312,7 +296,7 @@ int moe_router_topk(const void* logits, int logits_is_bf16, int ld, int T, int E
 
 size_t moe_dispatch_workspace_size(int T, int k, int E) {
     if (T < 0 || k < 1 || E < 1) return 0;
-    return kWsAlign + align_up(sizeof(int32_t) * (E + 1), kWsAlign) +
+    return kWsHead + align_up(sizeof(int32_t) * (E + 1), kWsAlign) +
            dispatch_scratch_bytes(T * k, E);
 }
 
@@ -339,7 +323,7 @@ size_t moe_expert_mlp_workspace_size(int T, int k, int E, int H, int I) {
     b.take<int32_t>(E + 1);
     GemvBufs gv;
     GemmBufs gm;
-    carve_gemv(a, T, k, H, I, 0, true, gv);
+    carve_gemv(a, T, k, H, I, 0, gv);
     carve_gemm(b, T, k, E, H, I, 0, gm);
     return std::max(a.size(), b.size());
 }
@@ -361,15 +345,16 @@ int moe_expert_mlp(const uint16_t* x, int T, int k, const moe_experts* W, const 
     int32_t* active = c.take<int32_t>(W->E + 1);
     {
         KernelScope ks_("active_from_offsets", st);
-        active_from_offsets_kernel<<<1, 256, 0, st>>>(offsets, W->E, active, active + W->E);
+        if (launch_pdl(active_from_offsets_kernel, dim3(1), dim3(256), 0, st, offsets, W->E, active, active + W->E) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
     }
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     MlpCall mc{};
     mc.x = x; mc.T = T; mc.k = k; mc.W = W; mc.sh = nullptr; mc.offsets = offsets; mc.perm = perm;
     mc.active = active; mc.n_active = active + W->E; mc.rows_out = rows; mc.status = static_cast<int*>(ws);
     if (a == MOE_ARM_GEMV) {
         GemvBufs b;
-        carve_gemv(c, T, k, W->H, W->I, 0, true, b);
+        carve_gemv(c, T, k, W->H, W->I, 0, b);
         return run_gemv(mc, b, false, st);
     }
     GemmBufs b;
@@ -397,7 +382,7 @@ size_t moe_workspace_size(int T, int E, int k, int H, int I, int I_sh) {
     carve_routing(b, T, E, k, r);
     GemvBufs gv;
     GemmBufs gm;
-    carve_gemv(a, T, k, H, I, I_sh, T > MOE_MAX_T_GEMV_COMBINE, gv);
+    carve_gemv(a, T, k, H, I, I_sh, gv);
     carve_gemm(b, T, k, E, H, I, I_sh, gm);
     return std::max(a.size(), b.size());
 }
@@ -427,33 +412,46 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     float* w = topk_w_out ? topk_w_out : r.w;
     const uint16_t* g = sh ? sh->g : nullptr;
     const int ld = W->E + (g ? 1 : 0);
-    if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active, r.disp_scratch,
-                        status, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
     MlpCall mc{};
     mc.x = x; mc.T = T; mc.k = k; mc.W = W; mc.sh = sh; mc.logits = r.logits; mc.logit_ld = ld;
     mc.offsets = r.offsets; mc.perm = r.perm; mc.inv = r.inv; mc.active = r.active; mc.n_active = r.n_active;
     mc.topk_w = w; mc.residual = residual; mc.rows_out = nullptr; mc.y = y; mc.status = status;
     if (a == MOE_ARM_GEMV) {
-        const bool fused = T <= MOE_MAX_T_GEMV_COMBINE;
         GemvBufs b;
-        carve_gemv(c, T, k, W->H, W->I, I_sh, !fused, b);
-        return run_gemv(mc, b, fused, st);
+        carve_gemv(c, T, k, W->H, W->I, I_sh, b);
+        // decode batches: 4 launches -- logits (+ x quantisation), top-k + dispatch, gate/up, down + combine
+        const bool fused_routing = T <= 32;
+        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H)) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (fused_routing) {
+            if (launch_topk_dispatch(r.logits, ld, T, W->E, k, ids, w, r.counts, r.offsets, r.perm, r.inv, r.active,
+                                     r.n_active, status, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        } else {
+            if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
+            if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active,
+                                r.disp_scratch, status, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        return run_gemv(mc, b, true, st);
     }
+    if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active, r.disp_scratch,
+                        status, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
     GemmBufs b;
     carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
     return run_gemm(mc, b, st);
 }
 
 int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
-    if (!ws || ws_bytes < kWsAlign) return MOE_ERR_INVALID_ARG;
-    return status_of(cudaMemsetAsync(ws, 0, kWsAlign, S(stream)));
+    if (!ws || ws_bytes < kWsHead) return MOE_ERR_INVALID_ARG;
+    return status_of(cudaMemsetAsync(ws, 0, kWsHead, S(stream)));
 }
 
 int moe_device_status(void* ws, size_t ws_bytes, int* status, moe_stream_t stream) {
-    if (!ws || !status || ws_bytes < kWsAlign) return MOE_ERR_INVALID_ARG;
+    if (!ws || !status || ws_bytes < kWsHead) return MOE_ERR_INVALID_ARG;
     int host = 0;
     cudaStream_t st = S(stream);
     if (cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;

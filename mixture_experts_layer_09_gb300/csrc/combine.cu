@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const float* __restrict__ shared,
                                                       const uint16_t* __restrict__ residual, int T, int k,
                                                       int H, float* __restrict__ y) {
+    pdl_wait();
+    pdl_trigger();
     const int H4 = H / 4;
     const long total = static_cast<long>(T) * H4;
     for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -58,13 +60,10 @@ cudaError_t launch_combine(const float* rows, const int32_t* inv, const float* t
     long blocks = (total + 255) / 256;
     if (blocks > 152L * 16) blocks = 152L * 16;
     KernelScope ks_("combine", st);
+    const dim3 grid(static_cast<unsigned>(blocks)), block(256);
     if (weighted_slots)
-        combine_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(rows, inv, topk_w, shared, residual,
-                                                                            T, k, H, y);
-    else
-        combine_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(rows, inv, topk_w, shared, residual,
-                                                                             T, k, H, y);
-    return cudaGetLastError();
+        return launch_pdl(combine_kernel<true>, grid, block, 0, st, rows, inv, topk_w, shared, residual, T, k, H, y);
+    return launch_pdl(combine_kernel<false>, grid, block, 0, st, rows, inv, topk_w, shared, residual, T, k, H, y);
 }
 
 }  // namespace moe

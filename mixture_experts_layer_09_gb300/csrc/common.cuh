@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 #if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ < 1000)
@@ -15,6 +17,11 @@ namespace moe {
 
 constexpr int kWarp = 32;
 constexpr size_t kWsAlign = 256;
+// Head of every workspace: the device status word at offset 0 and, from kWsCounterOffset,
+// the per-column-block counters of the GEMV down projection (zero between calls).
+constexpr size_t kWsHead = 4096;
+constexpr size_t kWsCounterOffset = 1024;
+constexpr int kMaxColBlocks = static_cast<int>((kWsHead - kWsCounterOffset) / sizeof(int));  // H <= 24576
 
 // Device status word layout (first 256 bytes of every workspace).
 struct DevStatus {
@@ -67,5 +74,29 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
 }
 
 __host__ __device__ constexpr inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Programmatic dependent launch.  Every kernel of the library is launched with programmatic
+// stream serialisation, so it may start while the previous kernel of the stream drains; it
+// must call pdl_wait() before it reads or writes any memory that earlier work touches.  Once
+// pdl_wait() returns, every earlier kernel of the stream has completed and its writes are
+// visible.  pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace moe

@@ -15,6 +15,7 @@
 // one slot (ascending) and its length; the expert kernels iterate over that list.
 #include "common.cuh"
 #include "internal.h"
+#include "route_core.cuh"
 
 namespace moe {
 
@@ -23,104 +24,12 @@ constexpr int kBigWarps = 8;          // warps per CTA in the multi-CTA path
 constexpr int kBigSlotsPerWarp = 256;  // slots per warp in the multi-CTA path
 constexpr int kBigSlotsPerCta = kBigWarps * kBigSlotsPerWarp;
 
-// Walk a warp's slot run 32 at a time.  mode 0: count into hist; mode 1: scatter using hist
-// as the running base (hist must hold the warp's starting position per expert).
-__device__ __forceinline__ void warp_walk(const int32_t* __restrict__ ids, int begin, int end, int E,
-                                          int* hist, int mode, int32_t* __restrict__ perm,
-                                          int32_t* __restrict__ inv, int* status) {
-    const int lane = threadIdx.x & 31;
-    const unsigned lt = lanemask_lt();
-    for (int base = begin; base < end; base += 32) {
-        const int a = base + lane;
-        int id = -1;
-        if (a < end) {
-            id = __ldg(ids + a);
-            if (id < 0 || id >= E) {
-                if (mode == 0) record_status(status, MOE_ERR_DEVICE_INDEX, a, id);
-                id = -1;
-            }
-        }
-        const unsigned peers = __match_any_sync(0xffffffffu, id);
-        const int leader = __ffs(peers) - 1;
-        if (mode == 0) {
-            if (id >= 0 && lane == leader) hist[id] += __popc(peers);
-        } else {
-            int pos = -1;
-            if (id >= 0) pos = hist[id] + __popc(peers & lt);
-            __syncwarp();
-            if (id >= 0 && lane == leader) hist[id] += __popc(peers);
-            if (a < end) {
-                if (id >= 0) perm[pos] = a;
-                inv[a] = pos;
-            }
-        }
-        __syncwarp();
-    }
-}
-
-// Exclusive scan of v over threads 0..255 (v = 0 for threads >= n); returns the prefix and
-// writes the total to *total.  Uses scratch[8 + 1].
-__device__ __forceinline__ int cta_exclusive_scan_256(int v, int* scratch, int* total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (threadIdx.x < 256 && lane == 31) scratch[w] = incl;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int run = 0;
-        for (int i = 0; i < 8; ++i) {
-            const int tmp = scratch[i];
-            scratch[i] = run;
-            run += tmp;
-        }
-        scratch[8] = run;
-    }
-    __syncthreads();
-    const int res = (threadIdx.x < 256) ? scratch[w] + incl - v : 0;
-    *total = scratch[8];
-    __syncthreads();
-    return res;
-}
-
-// After per-(warp or CTA) counts are known: counts, offsets, active list, and turns the
-// count table cnt[rows][E] into starting positions.  Needs blockDim.x >= 256.
-__device__ void finalize_plan(int* cnt, int rows, int E, int n, int32_t* counts, int32_t* offsets,
-                              int32_t* active, int32_t* n_active, int* scratch) {
-    const int e = threadIdx.x;
-    int total = 0;
-    if (e < E) {
-        for (int r = 0; r < rows; ++r) {
-            const int tmp = cnt[static_cast<size_t>(r) * E + e];
-            cnt[static_cast<size_t>(r) * E + e] = total;
-            total += tmp;
-        }
-    }
-    int sum;
-    const int off = cta_exclusive_scan_256(e < E ? total : 0, scratch, &sum);
-    const int flag = (e < E && total > 0) ? 1 : 0;
-    int nact;
-    const int apos = cta_exclusive_scan_256(flag, scratch, &nact);
-    if (e < E) {
-        offsets[e] = off;
-        if (counts) counts[e] = total;
-        for (int r = 0; r < rows; ++r) cnt[static_cast<size_t>(r) * E + e] += off;
-        if (flag) active[apos] = e;
-    }
-    if (threadIdx.x == 0) {
-        offsets[E] = sum;
-        *n_active = nact;
-    }
-    (void)n;
-}
-
 // One CTA of 1024 threads (32 warps) for T*k <= kSmallSlots.
 __global__ void __launch_bounds__(1024) dispatch_small_kernel(
     const int32_t* __restrict__ ids, int n, int E, int32_t* counts, int32_t* offsets, int32_t* perm,
     int32_t* inv, int32_t* active, int32_t* n_active, int* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int hist[];  // [32][E]
     __shared__ int scratch[9];
     const int w = threadIdx.x >> 5;
@@ -138,6 +47,8 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
 // Multi-CTA path, phase 1: per-CTA histogram.
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
     const int32_t* __restrict__ ids, int n, int E, int* __restrict__ cta_cnt, int* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int hist[];  // [kBigWarps][E]
     const int w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kBigWarps * E; i += blockDim.x) hist[i] = 0;
@@ -157,6 +68,8 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
 __global__ void __launch_bounds__(256) dispatch_scan_kernel(int* cta_cnt, int nblk, int E, int n,
                                                             int32_t* counts, int32_t* offsets,
                                                             int32_t* active, int32_t* n_active) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int scratch[9];
     finalize_plan(cta_cnt, nblk, E, n, counts, offsets, active, n_active, scratch);
 }
@@ -165,6 +78,8 @@ __global__ void __launch_bounds__(256) dispatch_scan_kernel(int* cta_cnt, int nb
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     const int32_t* __restrict__ ids, int n, int E, const int* __restrict__ cta_base, int32_t* perm,
     int32_t* inv, int* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ int hist[];  // [kBigWarps][E]
     const int w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kBigWarps * E; i += blockDim.x) hist[i] = 0;
@@ -185,6 +100,58 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     warp_walk(ids, begin, end, E, hist + w * E, 1, perm, inv, status);
 }
 
+// Decode batches (T <= 32): one CTA computes the top-k of every token (warp t takes token t)
+// and then the dispatch of the fresh ids -- stages 1 and 2 in one launch.
+template <int VPT>
+__global__ void __launch_bounds__(1024) topk_dispatch_kernel(const float* __restrict__ logits, int ld, int T, int E,
+                                                             int k, int32_t* ids, float* w, int32_t* counts,
+                                                             int32_t* offsets, int32_t* perm, int32_t* inv,
+                                                             int32_t* active, int32_t* n_active, int* status) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ int hist[];  // [32][E]
+    __shared__ int scratch[9];
+    const int wid = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) hist[i] = 0;
+    if (wid < T)
+        topk_warp_row<float, VPT>(logits + static_cast<size_t>(wid) * ld, E, k, ids + static_cast<size_t>(wid) * k,
+                                  w + static_cast<size_t>(wid) * k);
+    __syncthreads();  // the ids written above are visible to the whole CTA from here
+    const int n = T * k;
+    const int per = ((n + 31) / 32 + 31) / 32 * 32;
+    const int begin = min(n, wid * per), end = min(n, begin + per);
+    warp_walk(ids, begin, end, E, hist + wid * E, 0, perm, inv, status);
+    __syncthreads();
+    finalize_plan(hist, 32, E, n, counts, offsets, active, n_active, scratch);
+    __syncthreads();
+    warp_walk(ids, begin, end, E, hist + wid * E, 1, perm, inv, status);
+}
+
+cudaError_t launch_topk_dispatch(const float* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                                 int32_t* n_active, int* status, cudaStream_t st) {
+    const size_t smem = 32 * E * sizeof(int);
+    const int vpt = (E + 31) / 32;
+    KernelScope ks_("topk_dispatch", st);
+    switch (vpt) {
+#define MOE_TD_CASE(V)                                                                                            \
+    case V:                                                                                                       \
+        return launch_pdl(topk_dispatch_kernel<V>, dim3(1), dim3(1024), smem, st, logits, ld, T, E, k, ids, w,  \
+                          counts, offsets, perm, inv, active, n_active, status);
+        MOE_TD_CASE(1)
+        MOE_TD_CASE(2)
+        MOE_TD_CASE(3)
+        MOE_TD_CASE(4)
+        MOE_TD_CASE(5)
+        MOE_TD_CASE(6)
+        MOE_TD_CASE(7)
+        MOE_TD_CASE(8)
+#undef MOE_TD_CASE
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
 size_t dispatch_scratch_bytes(int n, int E) {
     if (n <= kSmallSlots) return 0;
     const size_t nblk = (n + kBigSlotsPerCta - 1) / kBigSlotsPerCta;
@@ -198,27 +165,30 @@ cudaError_t launch_dispatch(const int32_t* ids, int n, int E, int32_t* counts, i
         const size_t smem = 32 * E * sizeof(int);
         {
             KernelScope ks_("dispatch_small", st);
-            dispatch_small_kernel<<<1, 1024, smem, st>>>(ids, n, E, counts, offsets, perm, inv, active, n_active,
-                                                         status);
+            return launch_pdl(dispatch_small_kernel, dim3(1), dim3(1024), smem, st, ids, n, E, counts, offsets, perm,
+                              inv, active, n_active, status);
         }
-        return cudaGetLastError();
     }
     const int nblk = (n + kBigSlotsPerCta - 1) / kBigSlotsPerCta;
     int* cnt = static_cast<int*>(scratch);
     const size_t smem = kBigWarps * E * sizeof(int);
     {
         KernelScope ks_("dispatch_count", st);
-        dispatch_count_kernel<<<nblk, kBigWarps * 32, smem, st>>>(ids, n, E, cnt, status);
+        cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, cnt,
+                                   status);
+        if (e != cudaSuccess) return e;
     }
     {
         KernelScope ks_("dispatch_scan", st);
-        dispatch_scan_kernel<<<1, 256, 0, st>>>(cnt, nblk, E, n, counts, offsets, active, n_active);
+        cudaError_t e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, st, cnt, nblk, E, n, counts, offsets,
+                                   active, n_active);
+        if (e != cudaSuccess) return e;
     }
     {
         KernelScope ks_("dispatch_scatter", st);
-        dispatch_scatter_kernel<<<nblk, kBigWarps * 32, smem, st>>>(ids, n, E, cnt, perm, inv, status);
+        return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E,
+                          static_cast<const int*>(cnt), perm, inv, status);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -25,6 +25,7 @@
 // memory and returns.
 #include <cuda.h>
 
+#include "async.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,7 +38,6 @@ constexpr int kTileBytesA = BM * BK * 2;
 constexpr int kTileBytesB = BN * BK * 2;
 constexpr int kStagesGU = 4;
 constexpr int kStagesDN = 6;
-constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at 2 GHz
 
 struct GemmK {
     CUtensorMap tm_r;     // B operand of routed tiles
@@ -71,65 +71,6 @@ struct GemmK {
     int* status;
 };
 
-// ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait: false when the CTA is aborting or the limit ran out (then it records the
-// timeout and raises the abort flag for every role of the CTA).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int where) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t spin = 1;; ++spin) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 255) == 0) {
-            if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
-                *abort_flag = 1;
-                record_status(status, MOE_ERR_DEVICE_TIMEOUT, where, static_cast<int>(blockIdx.x));
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -248,6 +189,8 @@ __device__ __forceinline__ void store_dequant(uint8_t* tile, int row, const RawK
 
 template <int MODE>  // 0 = gate+up (two accumulators, SwiGLU epilogue), 1 = down
 __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ GemmK p) {
+    pdl_wait();
+    pdl_trigger();
     constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
     constexpr int NMAT = MODE == 0 ? 2 : 1;
     constexpr int kStageBytes = NMAT * kTileBytesA + kTileBytesB;
@@ -466,6 +409,8 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
 // Tile list from the bucket offsets: tiles of up to BN rows per expert, expert-major.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ offsets, int E,
                                                           int* __restrict__ tiles, int* __restrict__ n_tiles) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_tot[8];
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
     const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
@@ -491,6 +436,8 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int T, int k, int H,
                                                           int with_tokens, uint16_t* __restrict__ x16) {
+    pdl_wait();
+    pdl_trigger();
     const int n_rows = T * k + (with_tokens ? T : 0);
     const int H8 = H / 8;
     const long total = static_cast<long>(n_rows) * H8;
@@ -512,34 +459,10 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 }
 
 // ------------------------------------------------------------------ host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(ptr);
-    }();
-    return fn;
-}
-
 // 2D fp16 tensor [rows][K], box = 64 x BN, 128-byte swizzle, zero fill outside.
 static bool make_tmap(CUtensorMap* m, const void* base, int K, int rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows < 1 ? 1 : rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {BK, BN};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
+                   static_cast<uint64_t>(K) * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int gemm_ntile_max(int n_slots, int E) { return (n_slots + BN - 1) / BN + E; }
@@ -576,16 +499,18 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
         if (blocks < 1) blocks = 1;
         {
             KernelScope ks_("gather_rows", st);
-            gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p.x, p.perm, p.T, p.k, p.H, has_sh ? 1 : 0,
-                                                                             p.x16);
+            err = launch_pdl(gather_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, p.x, p.perm,
+                             p.T, p.k, p.H, has_sh ? 1 : 0, p.x16);
         }
     }
     // 2. tile schedule
     {
         KernelScope ks_("build_tiles", st);
-        build_tiles_kernel<<<1, 256, 0, st>>>(p.offsets, p.E, p.tiles, p.n_tiles);
+        if (err == cudaSuccess)
+            err = launch_pdl(build_tiles_kernel, dim3(1), dim3(256), 0, st, static_cast<const int32_t*>(p.offsets), p.E,
+                             p.tiles, p.n_tiles);
     }
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (err != cudaSuccess) return err;
 
     // 3. gate + up
     GemmK g{};
@@ -624,9 +549,9 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
         const int ctas = g.ctas_r + (has_sh ? p.sh_tiles * g.mblk_s : 0);
         {
             KernelScope ks_("gemm_gateup", st);
-            moe_gemm_kernel<0><<<ctas, 192, gemm_smem_bytes<0>(), st>>>(g);
+            err = launch_pdl(moe_gemm_kernel<0>, dim3(ctas), dim3(192), gemm_smem_bytes<0>(), st, g);
         }
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (err != cudaSuccess) return err;
     }
     // 4. down (+ weighting / shared gate in the epilogue)
     GemmK d = g;
@@ -659,9 +584,9 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
         const int ctas = d.ctas_r + (has_sh ? p.sh_tiles * d.mblk_s : 0);
         {
             KernelScope ks_("gemm_down", st);
-            moe_gemm_kernel<1><<<ctas, 192, gemm_smem_bytes<1>(), st>>>(d);
+            err = launch_pdl(moe_gemm_kernel<1>, dim3(ctas), dim3(192), gemm_smem_bytes<1>(), st, d);
         }
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        if (err != cudaSuccess) return err;
     }
     return cudaSuccess;
 }

@@ -3,36 +3,38 @@
 // The expert weights are int4 offset-binary (value = nibble - 8) with one fp16 scale per 32
 // K-columns, uploaded in the CPU byte layout (colibri PR #418 "Vulkan backend: expert tier +
 // dense + MLA attention on any Vulkan 1.2 GPU", Correctness and "Grouped scales in the Vulkan
-// kernels": the scale is applied to the packed-word partial).  A lane streams one 16-byte
-// chunk of a weight row = 32 nibbles = exactly one scale group, so the partial of a chunk is
+// kernels": the scale is applied to the packed-word partial).  A 16-byte chunk of a weight
+// row is 32 nibbles = exactly one scale group, so the partial of a chunk is
 //     sum_c (n_c - 8) * a_c  =  sum_c n_c * a_c  -  8 * sum_c a_c
-// and the group scale multiplies that partial.  The activations a (hidden rows x, and the
-// SwiGLU product h for the down projection) are first written as int16 with one power-of-two
-// scale per 32 values, so sum_c n_c * a_c is an exact integer dot product (dp2a: two int16 by
-// two 8-bit nibbles per instruction) and the only rounding is the activation's: bf16 hidden
-// values within 2^7 of their group's largest magnitude convert exactly, smaller ones round at
-// 2^-15 of that magnitude; fp32 h rounds at 2^-15 of its group's largest magnitude.
+// and the group scale multiplies that partial.  Activations a (hidden rows x; the SwiGLU
+// product h for the down projection) are held as int16 with one power-of-two scale per 32
+// values, so sum_c n_c * a_c is an exact integer dot product (dp2a: two int16 by two 8-bit
+// nibbles per instruction).  The only rounding is the activation's: bf16 hidden values within
+// 2^7 of their group's largest magnitude convert exactly, smaller ones round at 2^-15 of it;
+// h rounds at 2^-15 of its group's largest magnitude.
 //
-// Kernels:
-//   quantize_rows    bf16 or fp32 rows -> int16 (dp2a order) + scale + integer sum per group
-//   gateup_gemv      one warp per (active expert, row i): g = W_g x, u = W_u x for the
-//                    expert's bucket, h = silu(g) * u (fp32)
-//   down_gemv        one CTA per NR output rows; its warps cover (row, active expert) pairs;
-//                    mode ROWS writes o per dispatched row; mode COMBINE keeps w * o per
-//                    (token, slot) in shared memory and sums shared row, slots by j and the
-//                    residual in that order (daScript PR #3988 "dasLLAMA vulkan: a MoE that
-//                    fits the card ...", combine-folded residual commit).
-// The shared expert, when present, is one more "expert" whose bucket is every token.
+// Work layout (both kernels): a CTA owns 32 consecutive weight rows of one expert; each of its
+// 8 warps owns 4 of them, with 8 lanes per row splitting the row's chunks, so every 128-bit
+// load instruction of a warp reads 4 rows x 128 contiguous bytes.
+//   gateup_gemv   g = W_g x, u = W_u x for the expert's bucket, h = silu(g) * u; the 32 rows
+//                 of a CTA are one quantisation group of h, so h is written directly as int16
+//                 with its scale and integer sum.
+//   down_gemv     o = W_d h for the bucket.  Mode ROWS writes o per dispatched row; mode
+//                 COMBINE writes w * o per (token, slot) and the gated shared row, and the
+//                 last CTA to finish a block of 32 output columns sums, per token, the shared
+//                 row, then the slots in order j, then the residual (daScript PR #3988
+//                 "dasLLAMA vulkan: a MoE that fits the card ...", combine-folded residual
+//                 commit) -- the combine runs inside the down projection's launch.
+// The shared expert, when present, is one more expert whose bucket is every token.
 #include <algorithm>
 
+#include "async.cuh"
 #include "common.cuh"
 #include "internal.h"
+#include "quant.cuh"
 
 namespace moe {
 
-// position of column j (0..7) of an 8-column word in the dp2a operand order
-// [c0 c2 c4 c6 c1 c3 c5 c7]
-__device__ __forceinline__ int dp2a_pos(int j) { return (j & 1) ? 4 + (j >> 1) : (j >> 1); }
 
 // ------------------------------------------------------------------ activation quantisation
 struct QuantSeg {
@@ -40,11 +42,14 @@ struct QuantSeg {
     int is_bf16;
     int rows, K;
     int16_t* q;       // [rows][K], dp2a order within each 8-column word
-    float* sc;        // [rows][K/32]
-    int* sum;         // [rows][K/32]
+    int2* meta;       // [rows][gld] {scale bits, integer sum}
+    int gld;          // group row stride (>= K/32)
+    int kc;           // slice width of the stored order
 };
 
 __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantSeg s0, QuantSeg s1) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     long gw = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const long n0 = static_cast<long>(s0.rows) * (s0.K / 32);
@@ -61,409 +66,560 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(QuantSeg s0, QuantSe
     const size_t idx = static_cast<size_t>(row) * s.K + grp * 32 + lane;
     const float v = s.is_bf16 ? bf16_to_f32(static_cast<const uint16_t*>(s.src)[idx])
                               : static_cast<const float*>(s.src)[idx];
-    const float amax = warp_max(fabsf(v));
-    int q = 0;
-    float scale = 1.f;
-    if (amax > 0.f && amax <= 3.0e38f) {
-        int ex;
-        frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1): |v| * 2^(15 - ex) < 2^15
-        q = __float2int_rn(ldexpf(v, 15 - ex));
-        q = max(-32767, min(32767, q));
-        scale = ldexpf(1.f, ex - 15);
-    }
-    const int dst = grp * 32 + (lane & ~7) + dp2a_pos(lane & 7);
-    s.q[static_cast<size_t>(row) * s.K + dst] = static_cast<int16_t>(q);
-    const int qs = __reduce_add_sync(0xffffffffu, q);
-    if (lane == 0) {
-        s.sc[row * ng + grp] = scale;
-        s.sum[row * ng + grp] = qs;
-    }
+    quantize_group(v, lane, s.q + static_cast<size_t>(row) * act_row(s.K), grp, s.kc, s.meta + row * s.gld + grp);
 }
 
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st) {
-    QuantSeg s0{a.src0, a.src0_bf16, a.rows0, a.K0, a.q0, a.sc0, a.sum0};
-    QuantSeg s1{a.src1, a.src1_bf16, a.rows1, a.K1, a.q1, a.sc1, a.sum1};
+    QuantSeg s0{a.src0, a.src0_bf16, a.rows0, a.K0, a.q0, a.meta0, a.gld0 ? a.gld0 : a.K0 / 32, a.kc0};
+    QuantSeg s1{a.src1, a.src1_bf16, a.rows1, a.K1, a.q1, a.meta1, a.gld1 ? a.gld1 : a.K1 / 32, a.kc1};
     if (!a.src1) { s1.rows = 0; s1.K = 32; }
     const long warps = static_cast<long>(s0.rows) * (s0.K / 32) + static_cast<long>(s1.rows) * (s1.K / 32);
     if (warps == 0) return cudaSuccess;
     const long blocks = (warps + 7) / 8;
-    {
-        KernelScope ks_("quantize_rows", st);
-        quantize_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(s0, s1);
-    }
-    return cudaGetLastError();
+    KernelScope ks_("quantize_rows", st);
+    return launch_pdl(quantize_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, s0, s1);
 }
 
 // ------------------------------------------------------------------ int4 x int16 chunk dot
-// w: 16 bytes = 4 words = 32 nibbles (columns 0..31 of a group);
-// a: the group's 32 int16 activations in dp2a order (64 bytes).
-__device__ __forceinline__ int dot_chunk(const uint4 w, const int16_t* __restrict__ a) {
-    const uint4* ap = reinterpret_cast<const uint4*>(a);
-    int acc = 0;
+struct Nib {  // one 16-byte weight chunk split into its even and odd nibble bytes
+    uint32_t lo[4], hi[4];
+};
+
+__device__ __forceinline__ Nib split_nibbles(const uint4 w) {
+    Nib n;
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        const uint4 av = __ldg(ap + m);
-        const uint32_t lo = ww[m] & 0x0F0F0F0Fu;
-        const uint32_t hi = (ww[m] >> 4) & 0x0F0F0F0Fu;
-        acc = __dp2a_lo(static_cast<int>(av.x), static_cast<int>(lo), acc);
-        acc = __dp2a_hi(static_cast<int>(av.y), static_cast<int>(lo), acc);
-        acc = __dp2a_lo(static_cast<int>(av.z), static_cast<int>(hi), acc);
-        acc = __dp2a_hi(static_cast<int>(av.w), static_cast<int>(hi), acc);
+        n.lo[m] = ww[m] & 0x0F0F0F0Fu;          // columns 8m + 0, 2, 4, 6
+        n.hi[m] = (ww[m] >> 4) & 0x0F0F0F0Fu;   // columns 8m + 1, 3, 5, 7
+    }
+    return n;
+}
+
+// sum over the 32 columns of a chunk of nibble * activation; a = 32 int16 in dp2a order.
+__device__ __forceinline__ int dot_nib(const Nib& n, const uint4 (&a)[4]) {
+    int acc = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        acc = __dp2a_lo(static_cast<int>(a[m].x), static_cast<int>(n.lo[m]), acc);
+        acc = __dp2a_hi(static_cast<int>(a[m].y), static_cast<int>(n.lo[m]), acc);
+        acc = __dp2a_lo(static_cast<int>(a[m].z), static_cast<int>(n.hi[m]), acc);
+        acc = __dp2a_hi(static_cast<int>(a[m].w), static_cast<int>(n.hi[m]), acc);
     }
     return acc;
 }
 
+__device__ __forceinline__ void load_act(const int16_t* p, uint4 (&a)[4]) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a[m] = __ldg(q + m);
+}
+
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
-// ------------------------------------------------------------------ gate + up + SwiGLU
-// Items: n_active * I routed rows, then I_sh shared rows.  CPL = 16-byte chunks per lane
-// (ceil(H / 1024)).  TB = tokens per accumulation pass.
-template <int CPL, int TB>
-__global__ void __launch_bounds__(256) gateup_gemv_kernel(GemvArgs p) {
-    const int lane = threadIdx.x & 31;
-    const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int nw = (gridDim.x * blockDim.x) >> 5;
-    const int n_act = *p.n_active;
-    const long n_routed = static_cast<long>(n_act) * p.I;
-    const long items = n_routed + (p.sh_I > 0 ? p.sh_I : 0);
-    const int nch = p.H / 32;
-    const int ng = nch;
+__device__ __forceinline__ float f16_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
-    auto setup = [&](long it, const uint8_t*& qg, const uint8_t*& qu, const uint16_t*& sg, const uint16_t*& su) {
-        if (it < n_routed) {
-            const int e = p.active[it / p.I];
-            const int i = static_cast<int>(it % p.I);
-            const size_t row = static_cast<size_t>(e) * p.I + i;
-            qg = p.gate_q + row * (p.H / 2);
-            qu = p.up_q + row * (p.H / 2);
-            sg = p.gate_s + row * ng;
-            su = p.up_s + row * ng;
-        } else {
-            const size_t row = static_cast<size_t>(it - n_routed);
-            qg = p.sh_gate_q + row * (p.H / 2);
-            qu = p.sh_up_q + row * (p.H / 2);
-            sg = p.sh_gate_s + row * ng;
-            su = p.sh_up_s + row * ng;
-        }
-    };
+// Sum over the 8 lanes that share a row (lanes 8q .. 8q+7).
+__device__ __forceinline__ float row_sum8(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    return v;
+}
 
-    uint4 ng_buf[CPL], nu_buf[CPL];
-    long it = gw;
-    if (it < items) {
-        const uint8_t *qg, *qu;
-        const uint16_t *sg, *su;
-        setup(it, qg, qu, sg, su);
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-            if (c < nch) {
-                ng_buf[j] = ldg_stream(qg + static_cast<size_t>(c) * 16);
-                nu_buf[j] = ldg_stream(qu + static_cast<size_t>(c) * 16);
-            }
-        }
-    }
-    for (; it < items; it += nw) {
-        uint4 wg[CPL], wu[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) { wg[j] = ng_buf[j]; wu[j] = nu_buf[j]; }
-        const uint8_t *qg, *qu;
-        const uint16_t *sg, *su;
-        setup(it, qg, qu, sg, su);
-        float fsg[CPL], fsu[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-            fsg[j] = (c < nch) ? __half2float(__ushort_as_half(__ldg(sg + c))) : 0.f;
-            fsu[j] = (c < nch) ? __half2float(__ushort_as_half(__ldg(su + c))) : 0.f;
-        }
-        // prefetch the next item's chunks
-        const long nit = it + nw;
-        if (nit < items) {
-            const uint8_t *qg2, *qu2;
-            const uint16_t *sg2, *su2;
-            setup(nit, qg2, qu2, sg2, su2);
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int c = lane + 32 * j;
-                if (c < nch) {
-                    ng_buf[j] = ldg_stream(qg2 + static_cast<size_t>(c) * 16);
-                    nu_buf[j] = ldg_stream(qu2 + static_cast<size_t>(c) * 16);
-                }
-            }
-        }
-        // bucket of this item
-        int rb, re, ldh, i;
-        float* hout;
-        const bool shared = it >= n_routed;
-        if (!shared) {
-            const int e = p.active[it / p.I];
-            i = static_cast<int>(it % p.I);
-            rb = p.offsets[e];
-            re = p.offsets[e + 1];
-            hout = p.h;
-            ldh = p.I;
-        } else {
-            i = static_cast<int>(it - n_routed);
-            rb = 0;
-            re = p.T;
-            hout = p.sh_h;
-            ldh = p.sh_I;
-        }
-        for (int r0 = rb; r0 < re; r0 += TB) {
-            float ag[TB], au[TB];
-#pragma unroll
-            for (int b = 0; b < TB; ++b) { ag[b] = 0.f; au[b] = 0.f; }
-#pragma unroll
-            for (int b = 0; b < TB; ++b) {
-                if (r0 + b < re) {
-                    const int t = shared ? (r0 + b) : (p.perm[r0 + b] / p.k);
-                    const int16_t* xq = p.xq + static_cast<size_t>(t) * p.H;
-                    const float* xs = p.xsc + static_cast<size_t>(t) * ng;
-                    const int* xsum = p.xsum + static_cast<size_t>(t) * ng;
-#pragma unroll
-                    for (int j = 0; j < CPL; ++j) {
-                        const int c = lane + 32 * j;
-                        if (c < nch) {
-                            const int16_t* a = xq + c * 32;
-                            const int s8 = 8 * __ldg(xsum + c);
-                            const float xsc = __ldg(xs + c);
-                            const int dg = dot_chunk(wg[j], a) - s8;
-                            const int du = dot_chunk(wu[j], a) - s8;
-                            ag[b] = fmaf(static_cast<float>(dg), fsg[j] * xsc, ag[b]);
-                            au[b] = fmaf(static_cast<float>(du), fsu[j] * xsc, au[b]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int b = 0; b < TB; ++b) {
-                const float g = warp_sum(ag[b]);
-                const float u = warp_sum(au[b]);
-                if (lane == b && r0 + b < re) hout[static_cast<size_t>(r0 + b) * ldh + i] = silu(g) * u;
-            }
-        }
+
+// ------------------------------------------------------------------ pipelined GEMV kernels
+// Persistent CTAs, two per SM.  Work is a list of tasks -- (expert, block of 32 weight rows)
+// -- split into contiguous ranges, one per CTA.  A producer warp walks its range and streams
+// each task in K-slices into a ring of shared-memory stages: TMA boxes of the 32 weight rows
+// (256 bytes x 32 rows per box) and of their fp16 scales, one bulk copy per bucket token of
+// its int16 activation slice and one of its {scale, sum} pairs, and a small header (task,
+// pass, token rows, slots, weights) written before the stage's mbarrier arrive.  Eight
+// consumer warps then work from shared memory only: warp w owns rows 4w .. 4w+3 of the task,
+// 8 lanes per row, lane % 8 taking chunks lane % 8, +8, +16, ... of the slice, so one weight
+// read covers 4 rows x 128 contiguous bytes and a row's sum meets by three shuffles.
+//
+// MODE 0 (gate/up): g = W_g x, u = W_u x, h = silu(g) * u; the 32 rows of a task are one
+//   quantisation group of h, so h is written as int16 with its scale and integer sum.
+// MODE 1 (down, combine): o = W_d h; w * o goes to the slot-ordered term buffer (the gated
+//   shared row to its own buffer).  Tasks run in column-block-major order; when a CTA leaves a
+//   block of 32 output columns it publishes how many of the block's tasks it did, and the CTA
+//   completing the block sums per token the shared row, the slots in order j and the residual
+//   (daScript PR #3988 "dasLLAMA vulkan: a MoE that fits the card ...", combine-folded
+//   residual commit).
+// MODE 2 (down, rows): o per dispatched row, unweighted.
+// The shared expert is one more expert whose bucket is every token.
+
+constexpr int kBoxB = 256;  // bytes of one weight TMA box row (512 K-columns)
+constexpr int kCW = 8;      // consumer warps
+
+template <int MODE>
+struct Pipe {
+    static constexpr int NMAT = (MODE == 0) ? 2 : 1;
+    static constexpr int KC = (MODE == 0) ? kSliceX : kSliceH;  // K columns per slice
+    static constexpr int NBOX = KC / 2 / kBoxB;         // weight boxes per matrix per slice
+    static constexpr int CPL = KC / 32 / 8;             // chunks per lane per slice
+    static constexpr int TB = 4;                         // tokens per pass
+    static constexpr int GRP = KC / 32;                  // scale groups per slice
+    static constexpr int WMAT = 32 * KC / 2;             // bytes of one matrix's slice
+    static constexpr int OFF_WS = NMAT * WMAT;
+    static constexpr int OFF_A = OFF_WS + NMAT * 32 * GRP * 2;
+    static constexpr int OFF_AM = OFF_A + TB * KC * 2;
+    static constexpr int OFF_HDR = OFF_AM + TB * GRP * 8;
+    static constexpr int STAGE = (OFF_HDR + 256 + 1023) / 1024 * 1024;
+    static constexpr int STAGES = (MODE == 0) ? 4 : 3;  // two CTAs fit one SM
+    static_assert(OFF_WS % 128 == 0 && OFF_A % 128 == 0 && OFF_AM % 16 == 0, "copy destinations aligned");
+};
+
+struct StageHdr {
+    int end;            // 1: no more work for this CTA
+    int shared, e, rb;  // task
+    int K, t0, nb;      // reduction length, first bucket row of the pass, tokens in the pass
+    int first, last;    // first / last slice of the pass
+    int task_end;       // this pass is the task's last
+    int sl;             // slice index
+    int arow[4];        // activation rows (tokens for gate/up, dispatch rows or tokens for down)
+    int slot[4];        // MODE 1 routed: slot a = perm[row]
+    float wgt[4];       // MODE 1: top-k weight of the slot, or the shared gate
+};
+
+struct TaskDesc {
+    bool shared;
+    int e, rb, K, b0, b1, wrow;
+};
+
+template <int MODE>
+__device__ __forceinline__ void task_desc(const GemvArgs& p, int t, int n_act, int nrb, TaskDesc& tk) {
+    const int routed = n_act * nrb;
+    const int rows_per_expert = (MODE == 0) ? p.I : p.H;
+    if (t < routed) {
+        tk.shared = false;
+        tk.rb = t % nrb;
+        tk.e = __ldg(p.active + t / nrb);
+        tk.b0 = __ldg(p.offsets + tk.e);
+        tk.b1 = __ldg(p.offsets + tk.e + 1);
+        tk.K = (MODE == 0) ? p.H : p.I;
+        tk.wrow = tk.e * rows_per_expert + tk.rb * 32;
+    } else {
+        tk.shared = true;
+        tk.e = -1;
+        tk.rb = t - routed;
+        tk.b0 = 0;
+        tk.b1 = p.T;
+        tk.K = (MODE == 0) ? p.H : p.sh_I;
+        tk.wrow = tk.rb * 32;
     }
 }
 
-// ------------------------------------------------------------------ down projection
-constexpr int kDownNR = 4;        // output rows per CTA
-constexpr int kDownWarps = 8;
-
-template <int CPL, int TB, bool COMBINE>
-__global__ void __launch_bounds__(kDownWarps * 32) down_gemv_kernel(GemvArgs p) {
-    extern __shared__ float contrib[];  // COMBINE: [NR][T*k] slot terms, then [NR][T] shared terms
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int n0 = blockIdx.x * kDownNR;
-    const int n_act = *p.n_active;
-    const bool has_sh = p.sh_I > 0;
-    const int items = kDownNR * (n_act + (has_sh ? 1 : 0));
-    const int TK = p.T * p.k;
-    float* slot_terms = contrib;
-    float* sh_terms = contrib + kDownNR * TK;
-    if (COMBINE) {
-        for (int i = threadIdx.x; i < kDownNR * (TK + p.T); i += blockDim.x) contrib[i] = 0.f;
-        __syncthreads();
+// MODE 1: publish `cnt` finished tasks of column block cb; the CTA that completes the block
+// sums, per token, the shared row, the slots in order and the residual, then resets the counter.
+__device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt, int n_act, int* last_flag) {
+    __threadfence();
+    named_barrier(1, kCW * 32);
+    if (threadIdx.x == 0) {
+        const int expected = n_act + (p.sh_I > 0 ? 1 : 0);
+        *last_flag = (atomicAdd(p.col_counter + cb, cnt) + cnt == expected);
     }
-
-    auto setup = [&](int it, const uint8_t*& q, const uint16_t*& s, int& K, int& n) {
-        const int rr = it % kDownNR;
-        const int ai = it / kDownNR;
-        n = n0 + rr;
-        if (ai < n_act) {
-            const int e = p.active[ai];
-            K = p.I;
-            const size_t row = static_cast<size_t>(e) * p.H + n;
-            q = p.down_q + row * (K / 2);
-            s = p.down_s + row * (K / 32);
-        } else {
-            K = p.sh_I;
-            q = p.sh_down_q + static_cast<size_t>(n) * (K / 2);
-            s = p.sh_down_s + static_cast<size_t>(n) * (K / 32);
+    named_barrier(1, kCW * 32);
+    if (*last_flag) {
+        __threadfence();
+        const int H = p.H;
+        for (int idx = threadIdx.x; idx < p.T * 32; idx += kCW * 32) {
+            const int tt = idx >> 5, nn = cb * 32 + (idx & 31);
+            float y = (p.sh_I > 0) ? __ldcg(p.sh_term + static_cast<size_t>(tt) * H + nn) : 0.f;
+            for (int j = 0; j < p.k; ++j) y += __ldcg(p.slot_term + (static_cast<size_t>(tt) * p.k + j) * H + nn);
+            if (p.residual) y += bf16_to_f32(p.residual[static_cast<size_t>(tt) * H + nn]);
+            p.y[static_cast<size_t>(tt) * H + nn] = y;
         }
-    };
-
-    uint4 nbuf[CPL];
-    int it = wid;
-    if (it < items) {
-        const uint8_t* q;
-        const uint16_t* s;
-        int K, n;
-        setup(it, q, s, K, n);
-        if (n < p.H) {
-#pragma unroll
-            for (int j = 0; j < CPL; ++j) {
-                const int c = lane + 32 * j;
-                if (c < K / 32) nbuf[j] = ldg_stream(q + static_cast<size_t>(c) * 16);
-            }
-        }
+        if (threadIdx.x == 0) p.col_counter[cb] = 0;  // ready for the next call
     }
-    for (; it < items; it += kDownWarps) {
-        uint4 w[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) w[j] = nbuf[j];
-        const uint8_t* q;
-        const uint16_t* s;
-        int K, n;
-        setup(it, q, s, K, n);
-        const int nch = K / 32;
-        const bool live = n < p.H;
-        float fs[CPL];
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-            const int c = lane + 32 * j;
-            fs[j] = (live && c < nch) ? __half2float(__ushort_as_half(__ldg(s + c))) : 0.f;
+    named_barrier(1, kCW * 32);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __grid_constant__ GemvArgs p) {
+    using P = Pipe<MODE>;
+    constexpr int NMAT = P::NMAT, S = P::STAGES, TB = P::TB;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * P::STAGE);
+    uint64_t* empty = full + S;
+    float* red = reinterpret_cast<float*>(empty + S);  // MODE 0: [TB][2][32]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + TB * 2 * 32);
+    int* last_flag = const_cast<int*>(abort_flag) + 1;
+
+    pdl_wait();
+    pdl_trigger();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kCW);
         }
-        const int nit = it + kDownWarps;
-        if (nit < items) {
-            const uint8_t* q2;
-            const uint16_t* s2;
-            int K2, n2;
-            setup(nit, q2, s2, K2, n2);
-            if (n2 < p.H) {
-#pragma unroll
-                for (int j = 0; j < CPL; ++j) {
-                    const int c = lane + 32 * j;
-                    if (c < K2 / 32) nbuf[j] = ldg_stream(q2 + static_cast<size_t>(c) * 16);
-                }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == kCW) {
+        // ---------------- producer
+        const int n_act = *p.n_active;
+        const int nrb = (MODE == 0) ? p.I / 32 : p.H / 32;
+        const int nsh = (p.sh_I > 0) ? ((MODE == 0) ? p.sh_I / 32 : p.H / 32) : 0;
+        const int ntask = n_act * nrb + nsh;
+        const int per_cb = n_act + (nsh > 0 ? 1 : 0);
+        const int len = (ntask + gridDim.x - 1) / gridDim.x;
+        const int first = blockIdx.x * len, last = min(ntask, first + len);
+        uint32_t it = 0;
+        for (int q0 = first; q0 < last && !*abort_flag; q0 += 32) {
+          // the warp's lanes look up the next 32 task descriptors at once
+          TaskDesc mine{};
+          if (q0 + lane < last) {
+              // MODE 1 walks column-block-major (block cb: experts in order, then the shared one)
+              int t = q0 + lane;
+              if (MODE == 1) {
+                  const int cb = t / per_cb, a = t % per_cb;
+                  t = a < n_act ? a * nrb + cb : n_act * nrb + cb;
+              }
+              task_desc<MODE>(p, t, n_act, nrb, mine);
+          }
+          const int wn = min(32, last - q0);
+          for (int j = 0; j < wn && !*abort_flag; ++j) {
+            TaskDesc tk;
+            tk.shared = __shfl_sync(0xffffffffu, static_cast<int>(mine.shared), j);
+            tk.e = __shfl_sync(0xffffffffu, mine.e, j);
+            tk.rb = __shfl_sync(0xffffffffu, mine.rb, j);
+            tk.K = __shfl_sync(0xffffffffu, mine.K, j);
+            tk.b0 = __shfl_sync(0xffffffffu, mine.b0, j);
+            tk.b1 = __shfl_sync(0xffffffffu, mine.b1, j);
+            tk.wrow = __shfl_sync(0xffffffffu, mine.wrow, j);
+            const CUtensorMap* tw[2];
+            const CUtensorMap* ts[2];
+            const int16_t* aq;
+            const int2* am;
+            int ag_ld, ws;
+            if (MODE == 0) {
+                tw[0] = tk.shared ? &p.tm_sh_gate : &p.tm_gate;
+                tw[1] = tk.shared ? &p.tm_sh_up : &p.tm_up;
+                ts[0] = tk.shared ? &p.tm_sh_gate_s : &p.tm_gate_s;
+                ts[1] = tk.shared ? &p.tm_sh_up_s : &p.tm_up_s;
+                ws = tk.shared ? p.ws_sh_gu : p.ws_gu;
+                aq = p.xq; am = p.xmeta; ag_ld = p.x_gld;
+            } else {
+                tw[0] = tw[1] = tk.shared ? &p.tm_sh_down : &p.tm_down;
+                ts[0] = ts[1] = tk.shared ? &p.tm_sh_down_s : &p.tm_down_s;
+                ws = tk.shared ? p.ws_sh_d : p.ws_d;
+                aq = tk.shared ? p.sh_hq : p.hq;
+                am = tk.shared ? p.sh_hmeta : p.hmeta;
+                ag_ld = tk.shared ? p.sh_gld : p.h_gld;
             }
-        }
-        if (!live) continue;
-        const int ai = it / kDownNR;
-        const int rr = it % kDownNR;
-        const bool shared = ai >= n_act;
-        int rb, re;
-        if (!shared) {
-            const int e = p.active[ai];
-            rb = p.offsets[e];
-            re = p.offsets[e + 1];
-        } else {
-            rb = 0;
-            re = p.T;
-        }
-        const int16_t* hq = shared ? p.sh_hq : p.hq;
-        const float* hsc = shared ? p.sh_hsc : p.hsc;
-        const int* hsum = shared ? p.sh_hsum : p.hsum;
-        for (int r0 = rb; r0 < re; r0 += TB) {
-            float acc[TB];
-#pragma unroll
-            for (int b = 0; b < TB; ++b) acc[b] = 0.f;
-#pragma unroll
-            for (int b = 0; b < TB; ++b) {
-                if (r0 + b < re) {
-                    const size_t r = static_cast<size_t>(r0 + b);
-                    const int16_t* a = hq + r * K;
-#pragma unroll
-                    for (int j = 0; j < CPL; ++j) {
-                        const int c = lane + 32 * j;
-                        if (c < nch) {
-                            const int d = dot_chunk(w[j], a + c * 32) - 8 * __ldg(hsum + r * nch + c);
-                            acc[b] = fmaf(static_cast<float>(d), fs[j] * __ldg(hsc + r * nch + c), acc[b]);
+            const int nsl = (tk.K + P::KC - 1) / P::KC;
+            for (int t0 = tk.b0; t0 < tk.b1 && !*abort_flag; t0 += TB) {
+                const int nb = min(TB, tk.b1 - t0);
+                int arow = 0, slot = 0;
+                float wgt = 0.f;
+                if (lane < nb) {
+                    const int r = t0 + lane;
+                    if (MODE == 0) {
+                        arow = tk.shared ? r : __ldg(p.perm + r) / p.k;
+                    } else {
+                        arow = r;
+                        if (tk.shared) {
+                            wgt = 1.f;
+                            if (p.sh_gate_logit)
+                                wgt = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
+                        } else if (MODE == 1) {
+                            slot = __ldg(p.perm + r);
+                            wgt = __ldg(p.topk_w + slot);
                         }
                     }
                 }
+                for (int sl = 0; sl < nsl; ++sl, ++it) {
+                    const int s = it % S;
+                    if (it >= static_cast<uint32_t>(S)) {
+                        // one lane waits; the warp takes its answer (uniform control flow)
+                        bool ok = true;
+                        if (lane == 0) ok = mbar_wait(empty + s, ((it / S) & 1) ^ 1, abort_flag, p.status, 11);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        __syncwarp();
+                        if (!ok) break;
+                    }
+                    uint8_t* st = smem + s * P::STAGE;
+                    StageHdr* hd = reinterpret_cast<StageHdr*>(st + P::OFF_HDR);
+                    if (lane == 0) {
+                        hd->end = 0; hd->shared = tk.shared; hd->e = tk.e; hd->rb = tk.rb; hd->K = tk.K;
+                        hd->t0 = t0; hd->nb = nb; hd->first = (sl == 0); hd->last = (sl == nsl - 1); hd->sl = sl;
+                        hd->task_end = (t0 + TB >= tk.b1);
+                    }
+                    if (lane < nb) {
+                        hd->arow[lane] = arow;
+                        hd->slot[lane] = slot;
+                        hd->wgt[lane] = wgt;
+                    }
+                    __syncwarp();
+                    const int cols = min(P::KC, tk.K - sl * P::KC);
+                    const uint32_t ab = act_row(cols) * 2;          // whole groups of 8 chunks
+                    const uint32_t mb = ((cols / 32 + 3) & ~3) * 8;  // {scale, sum} pairs, padded
+                    if (lane == 0) {
+                        const uint32_t bytes = NMAT * (P::WMAT + (ws ? 32 * P::GRP * 2 : 0)) + nb * (ab + mb);
+                        mbar_arrive_expect_tx(full + s, bytes);  // release: the header is visible
+#pragma unroll
+                        for (int m = 0; m < NMAT; ++m) {
+#pragma unroll
+                            for (int bx = 0; bx < P::NBOX; ++bx)
+                                tma_load_2d(st + m * P::WMAT + bx * 32 * kBoxB, tw[m], sl * (P::KC / 2) + bx * kBoxB,
+                                            tk.wrow, full + s);
+                            if (ws) tma_load_2d(st + P::OFF_WS + m * 32 * P::GRP * 2, ts[m], sl * P::GRP, tk.wrow, full + s);
+                        }
+                    }
+                    if (lane < nb) {
+                        bulk_load(st + P::OFF_A + lane * P::KC * 2,
+                                  aq + static_cast<size_t>(arow) * act_row(tk.K) + sl * P::KC, ab, full + s);
+                        bulk_load(st + P::OFF_AM + lane * P::GRP * 8, am + static_cast<size_t>(arow) * ag_ld + sl * P::GRP,
+                                  mb, full + s);
+                    }
+                }
             }
+          }
+        }
+        // closing stage: a header with end = 1 and no copies
+        if (!*abort_flag) {
+            const int s = it % S;
+            if (lane == 0 &&
+                (it < static_cast<uint32_t>(S) || mbar_wait(empty + s, ((it / S) & 1) ^ 1, abort_flag, p.status, 13))) {
+                reinterpret_cast<StageHdr*>(smem + s * P::STAGE + P::OFF_HDR)->end = 1;
+                mbar_arrive_expect_tx(full + s, 0);
+            }
+            ++it;
+        }
+        if (*abort_flag && lane == 0) {
+            // let the copies this warp started land before the CTA leaves (bounded)
+            const uint32_t f0 = it > static_cast<uint32_t>(S) ? it - S : 0;
+            for (uint32_t j = f0; j < it; ++j) {
+                const long long c0 = clock64();
+                while (!mbar_try_wait(full + j % S, (j / S) & 1) && clock64() - c0 < kWaitLimitCycles) {
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int ks = lane & 7;
+    const int lrow = 4 * warp + (lane >> 3);  // row of the task owned by this lane group
+    // scale rows for the direct path (when the scale rows cannot be staged by TMA)
+    const int n_act_c = (MODE == 1) ? *p.n_active : 0;
+    int run_cb = -1, run_cnt = 0;
+    float acc[TB][NMAT];
+    uint32_t it = 0;
+    for (;; ++it) {
+        const int s = it % S;
+        bool ok = true;
+        if (lane == 0) {
+            ok = mbar_wait(full + s, (it / S) & 1, abort_flag, p.status, 12);
+            if (!ok) {
+                // grace wait: if the stage does complete, every consumer warp goes on together,
+                // so no warp can be left alone at a named barrier; otherwise they all stop here
+                const long long c0 = clock64();
+                while (!(ok = mbar_try_wait(full + s, (it / S) & 1)) && clock64() - c0 < kWaitLimitCycles / 32) {
+                }
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        __syncwarp();  // lane 0's acquire of the stage is ordered before the warp's reads
+        const uint8_t* st = smem + s * P::STAGE;
+        const StageHdr* hd = reinterpret_cast<const StageHdr*>(st + P::OFF_HDR);
+        if (!ok || hd->end) break;
+        const int nb = hd->nb, K = hd->K, sl = hd->sl;
+        if (MODE == 1 && hd->rb != run_cb) {
+            if (run_cb >= 0) combine_flush(p, run_cb, run_cnt, n_act_c, last_flag);
+            run_cb = hd->rb;
+            run_cnt = 0;
+        }
+        if (hd->first) {
+#pragma unroll
+            for (int b = 0; b < TB; ++b)
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) acc[b][m] = 0.f;
+        }
+        const bool ws = hd->shared ? ((MODE == 0) ? p.ws_sh_gu : p.ws_sh_d) : ((MODE == 0) ? p.ws_gu : p.ws_d);
+        const int nch = min(P::KC, K - sl * P::KC) / 32;
+#pragma unroll
+        for (int j = 0; j < P::CPL; ++j) {
+            const int c = ks + 8 * j;  // chunk within the slice
+            if (c < nch) {
+                Nib nw[NMAT];
+                float fs[NMAT];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    nw[m] = split_nibbles(*reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB +
+                                                                          lrow * kBoxB + (c & 15) * 16));
+                    uint16_t sb;
+                    if (ws) {
+                        sb = *reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2);
+                    } else {
+                        const uint16_t* srow;
+                        const int rows_pe = (MODE == 0) ? p.I : p.H;
+                        if (MODE == 0)
+                            srow = hd->shared ? (m ? p.sh_up_s : p.sh_gate_s) : (m ? p.up_s : p.gate_s);
+                        else
+                            srow = hd->shared ? p.sh_down_s : p.down_s;
+                        const size_t wrow = hd->shared ? static_cast<size_t>(hd->rb) * 32 + lrow
+                                                       : static_cast<size_t>(hd->e) * rows_pe + hd->rb * 32 + lrow;
+                        sb = __ldg(srow + wrow * (K / 32) + sl * P::GRP + c);
+                    }
+                    fs[m] = f16_to_f32(sb);
+                }
+#pragma unroll
+                for (int b = 0; b < TB; ++b) {
+                    if (b < nb) {
+                        uint4 av[4];
+                        const uint4* ap = reinterpret_cast<const uint4*>(st + P::OFF_A + b * P::KC * 2);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
+                        const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
+                        const float asc = __int_as_float(amv.x);
+#pragma unroll
+                        for (int m = 0; m < NMAT; ++m)
+                            acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+                    }
+                }
+            }
+        }
+        // copy what the epilogue needs out of the header before the stage is released
+        const bool last = hd->last, shared = hd->shared, task_end = hd->task_end;
+        const int rb = hd->rb, t0 = hd->t0;
+        int slot[TB];
+        float wgt[TB];
+#pragma unroll
+        for (int b = 0; b < TB; ++b) {
+            slot[b] = hd->slot[b];
+            wgt[b] = hd->wgt[b];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + s);
+        if (!last) continue;
+        // ---- end of a pass
+        if (MODE == 0) {
+#pragma unroll
+            for (int b = 0; b < TB; ++b)
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    const float v = row_sum8(acc[b][m]);
+                    if (ks == 0) red[(b * 2 + m) * 32 + lrow] = v;
+                }
+            named_barrier(1, kCW * 32);
+            if (warp < nb) {
+                const int b = warp;
+                const float h = silu(red[(b * 2 + 0) * 32 + lane]) * red[(b * 2 + 1) * 32 + lane];
+                const int M = shared ? p.sh_I : p.I;
+                const int gld = shared ? p.sh_gld : p.h_gld;
+                int16_t* hq = shared ? p.sh_hq : p.hq;
+                int2* hm = shared ? p.sh_hmeta : p.hmeta;
+                const size_t rr = static_cast<size_t>(t0 + b);
+                quantize_group(h, lane, hq + rr * act_row(M), rb, kSliceH, hm + rr * gld + rb);
+            }
+            named_barrier(1, kCW * 32);
+        } else {
+            const int n = rb * 32 + lrow;  // output column of this lane group
 #pragma unroll
             for (int b = 0; b < TB; ++b) {
-                const float o = warp_sum(acc[b]);
-                if (lane == b && r0 + b < re) {
-                    const int r = r0 + b;
-                    if (COMBINE) {
-                        if (shared) {
-                            float gate = 1.f;
-                            if (p.sh_gate_logit) {
-                                const float z = p.sh_gate_logit[static_cast<size_t>(r) * p.logit_ld];
-                                gate = 1.f / (1.f + expf(-z));
-                            }
-                            sh_terms[rr * p.T + r] = gate * o;
-                        } else {
-                            const int a = p.perm[r];
-                            slot_terms[rr * TK + a] = p.topk_w[a] * o;
-                        }
-                    } else if (shared) {
-                        float gate = 1.f;
-                        if (p.sh_gate_logit) {
-                            const float z = p.sh_gate_logit[static_cast<size_t>(r) * p.logit_ld];
-                            gate = 1.f / (1.f + expf(-z));
-                        }
-                        p.sh_rows_out[static_cast<size_t>(r) * p.H + n] = gate * o;
+                const float o = row_sum8(acc[b][0]);
+                if (ks == 0 && b < nb) {
+                    const int r = t0 + b;
+                    if (shared) {
+                        float* dst = (MODE == 1) ? p.sh_term : p.sh_rows_out;
+                        dst[static_cast<size_t>(r) * p.H + n] = wgt[b] * o;
+                    } else if (MODE == 1) {
+                        p.slot_term[static_cast<size_t>(slot[b]) * p.H + n] = wgt[b] * o;
                     } else {
                         p.rows_out[static_cast<size_t>(r) * p.H + n] = o;
                     }
                 }
             }
+            if (MODE == 1 && task_end) ++run_cnt;
         }
     }
-    if (!COMBINE) return;
-    __syncthreads();
-    // y[t][n] = shared term + slots in order j + residual
-    for (int idx = threadIdx.x; idx < kDownNR * p.T; idx += blockDim.x) {
-        const int rr = idx / p.T, t = idx % p.T;
-        const int n = n0 + rr;
-        if (n >= p.H) continue;
-        float y = has_sh ? sh_terms[rr * p.T + t] : 0.f;
-        for (int j = 0; j < p.k; ++j) y += slot_terms[rr * TK + t * p.k + j];
-        if (p.residual) y += bf16_to_f32(p.residual[static_cast<size_t>(t) * p.H + n]);
-        p.y[static_cast<size_t>(t) * p.H + n] = y;
+    if (MODE == 1 && run_cb >= 0 && !*abort_flag) combine_flush(p, run_cb, run_cnt, n_act_c, last_flag);
+}
+
+// Weight maps: uint8 [rows][K/2], box 256 bytes x 32 rows.  Scale maps: fp16 [rows][K/32],
+// box 32 x 32 rows, only when a scale row is a multiple of 16 bytes (K % 256 == 0) and the
+// pointer is 16-byte aligned; otherwise the consumers read scales directly.
+static bool weight_maps(CUtensorMap* wm, CUtensorMap* sm, int* ws, const uint8_t* q, const uint16_t* s, int rows,
+                        int K, int sbox) {
+    if (!tmap_2d(wm, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(rows),
+                 static_cast<uint64_t>(K / 2), kBoxB, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    *ws = (K % 256 == 0) && (reinterpret_cast<uintptr_t>(s) & 15u) == 0;
+    if (*ws && !tmap_2d(sm, CU_TENSOR_MAP_DATA_TYPE_UINT16, s, static_cast<uint64_t>(K / 32),
+                        static_cast<uint64_t>(rows), static_cast<uint64_t>(K / 32) * 2, sbox, 32,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+        return false;
+    if (!*ws) *sm = *wm;
+    return true;
+}
+
+bool gemv_tensor_maps(GemvArgs& p, int E) {
+    int ws_up = 0;
+    const int gb = Pipe<0>::GRP, db = Pipe<1>::GRP;
+    if (!weight_maps(&p.tm_gate, &p.tm_gate_s, &p.ws_gu, p.gate_q, p.gate_s, E * p.I, p.H, gb)) return false;
+    if (!weight_maps(&p.tm_up, &p.tm_up_s, &ws_up, p.up_q, p.up_s, E * p.I, p.H, gb)) return false;
+    p.ws_gu = p.ws_gu && ws_up;
+    if (!weight_maps(&p.tm_down, &p.tm_down_s, &p.ws_d, p.down_q, p.down_s, E * p.H, p.I, db)) return false;
+    if (p.sh_I > 0) {
+        if (!weight_maps(&p.tm_sh_gate, &p.tm_sh_gate_s, &p.ws_sh_gu, p.sh_gate_q, p.sh_gate_s, p.sh_I, p.H, gb))
+            return false;
+        if (!weight_maps(&p.tm_sh_up, &p.tm_sh_up_s, &ws_up, p.sh_up_q, p.sh_up_s, p.sh_I, p.H, gb)) return false;
+        p.ws_sh_gu = p.ws_sh_gu && ws_up;
+        if (!weight_maps(&p.tm_sh_down, &p.tm_sh_down_s, &p.ws_sh_d, p.sh_down_q, p.sh_down_s, p.H, p.sh_I, db))
+            return false;
+    } else {
+        p.tm_sh_gate = p.tm_gate; p.tm_sh_up = p.tm_up; p.tm_sh_down = p.tm_down;
+        p.tm_sh_gate_s = p.tm_gate_s; p.tm_sh_up_s = p.tm_up_s; p.tm_sh_down_s = p.tm_down_s;
+        p.ws_sh_gu = p.ws_sh_d = 0;
     }
+    return true;
 }
 
-static int cpl_for(int K) {
-    const int nch = K / 32;
-    const int c = (nch + 31) / 32;
-    if (c <= 1) return 1;
-    if (c <= 2) return 2;
-    if (c <= 4) return 4;
-    if (c <= 8) return 8;
-    return -1;
+template <int MODE>
+static size_t pipe_smem_bytes() {
+    using P = Pipe<MODE>;
+    return 1024 + static_cast<size_t>(P::STAGES) * P::STAGE + 2 * P::STAGES * sizeof(uint64_t) +
+           P::TB * 2 * 32 * sizeof(float) + 16;
 }
 
-bool gemv_supported(int H, int I, int I_sh) {
-    return cpl_for(H) > 0 && cpl_for(I) > 0 && (I_sh <= 0 || cpl_for(I_sh) > 0);
+template <int MODE>
+static cudaError_t pipe_attr() {
+    static cudaError_t once = cudaFuncSetAttribute(gemv_pipe_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(pipe_smem_bytes<MODE>()));
+    return once;
 }
 
-cudaError_t launch_gateup_gemv(const GemvArgs& p, int num_sms, cudaStream_t st) {
-    const int cpl = cpl_for(p.H);
-    // enough warps to cover every (expert, row) item of a full decode batch in one pass,
-    // capped at 16 resident CTAs of 8 warps per SM
-    long max_items = static_cast<long>(p.max_active) * p.I + (p.sh_I > 0 ? p.sh_I : 0);
-    long blocks = (max_items + 7) / 8;
-    blocks = std::min<long>(blocks, static_cast<long>(num_sms) * 8);
-    if (blocks < 1) blocks = 1;
-    const dim3 g(static_cast<unsigned>(blocks)), b(256);
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 148;
+    return n;
+}
+
+cudaError_t launch_gateup_gemv(const GemvArgs& p, cudaStream_t st) {
+    cudaError_t e = pipe_attr<0>();
+    if (e != cudaSuccess) return e;
+    const int tasks = p.max_active * (p.I / 32) + (p.sh_I > 0 ? p.sh_I / 32 : 0);
+    const int grid = std::max(1, std::min(tasks, 2 * sm_count()));
     KernelScope ks_("gateup_gemv", st);
-    switch (cpl) {
-        case 1: gateup_gemv_kernel<1, 4><<<g, b, 0, st>>>(p); break;
-        case 2: gateup_gemv_kernel<2, 4><<<g, b, 0, st>>>(p); break;
-        case 4: gateup_gemv_kernel<4, 4><<<g, b, 0, st>>>(p); break;
-        case 8: gateup_gemv_kernel<8, 2><<<g, b, 0, st>>>(p); break;
-        default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    return launch_pdl(gemv_pipe_kernel<0>, dim3(grid), dim3((kCW + 1) * 32), pipe_smem_bytes<0>(), st, p);
 }
 
 cudaError_t launch_down_gemv(const GemvArgs& p, bool combine, cudaStream_t st) {
-    int cpl = cpl_for(p.I);
-    if (p.sh_I > 0) cpl = std::max(cpl, cpl_for(p.sh_I));
-    const dim3 g((p.H + kDownNR - 1) / kDownNR), b(kDownWarps * 32);
-    const size_t smem = combine ? sizeof(float) * kDownNR * (static_cast<size_t>(p.T) * p.k + p.T) : 0;
+    cudaError_t e = combine ? pipe_attr<1>() : pipe_attr<2>();
+    if (e != cudaSuccess) return e;
+    const int tasks = (p.max_active + (p.sh_I > 0 ? 1 : 0)) * (p.H / 32);
+    const int grid = std::max(1, std::min(tasks, 2 * sm_count()));
     KernelScope ks_(combine ? "down_gemv_combine" : "down_gemv_rows", st);
-#define MOE_DOWN_CASE(C)                                                              \
-    case C:                                                                           \
-        if (combine)                                                                  \
-            down_gemv_kernel<C, 4, true><<<g, b, smem, st>>>(p);                      \
-        else                                                                          \
-            down_gemv_kernel<C, 4, false><<<g, b, smem, st>>>(p);                     \
-        break;
-    switch (cpl) {
-        MOE_DOWN_CASE(1)
-        MOE_DOWN_CASE(2)
-        MOE_DOWN_CASE(4)
-        MOE_DOWN_CASE(8)
-        default: return cudaErrorInvalidValue;
-    }
-#undef MOE_DOWN_CASE
-    return cudaGetLastError();
+    if (combine) return launch_pdl(gemv_pipe_kernel<1>, dim3(grid), dim3((kCW + 1) * 32), pipe_smem_bytes<1>(), st, p);
+    return launch_pdl(gemv_pipe_kernel<2>, dim3(grid), dim3((kCW + 1) * 32), pipe_smem_bytes<2>(), st, p);
 }
 
 }  // namespace moe

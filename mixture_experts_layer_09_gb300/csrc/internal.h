@@ -1,6 +1,7 @@
 // internal.h -- launchers shared between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -20,13 +21,25 @@ class KernelScope {
     int idx_;
 };
 
+// tmap.cu: 2D tensor map (inner dimension first), cached per parameter set.
+bool tmap_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint64_t inner, uint64_t rows,
+             uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 // router.cu
+// xq/xsc/xsum (optional): also quantise x for the GEMV arm in the same launch (decode batches).
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
-                                 int E, float* logits, cudaStream_t st);
+                                 int E, float* logits, cudaStream_t st, int16_t* xq = nullptr,
+                                 int2* xmeta = nullptr, int x_gld = 0);
+// group row stride of the quantised activations: K/32 rounded up to a multiple of 4
+inline int act_gld(int K) { return ((K / 32) + 3) & ~3; }
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
                                float* w, cudaStream_t st);
 
 // dispatch.cu
+// Decode batches (T <= 32): top-k of every token and the dispatch in one single-CTA launch.
+cudaError_t launch_topk_dispatch(const float* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                                 int32_t* n_active, int* status, cudaStream_t st);
 size_t dispatch_scratch_bytes(int n_slots, int E);
 cudaError_t launch_dispatch(const int32_t* ids, int n_slots, int E, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* scratch,
@@ -37,17 +50,23 @@ struct QuantArgs {
     const void* src0 = nullptr;
     int src0_bf16 = 0, rows0 = 0, K0 = 32;
     int16_t* q0 = nullptr;
-    float* sc0 = nullptr;
-    int* sum0 = nullptr;
+    int2* meta0 = nullptr;        // {scale bits, integer sum} per group
+    int gld0 = 0;                 // row stride of meta0 in groups (0: K/32)
+    int kc0 = 512;                // slice width of the stored order of q0
     const void* src1 = nullptr;
     int src1_bf16 = 0, rows1 = 0, K1 = 32;
     int16_t* q1 = nullptr;
-    float* sc1 = nullptr;
-    int* sum1 = nullptr;
+    int2* meta1 = nullptr;
+    int gld1 = 0;
+    int kc1 = 512;
 };
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st);
 
 struct GemvArgs {
+    // TMA maps of the weights (uint8, box 256 B x 32 rows) and scales (fp16, box 16 x 32 rows)
+    CUtensorMap tm_gate, tm_up, tm_down, tm_gate_s, tm_up_s, tm_down_s;
+    CUtensorMap tm_sh_gate, tm_sh_up, tm_sh_down, tm_sh_gate_s, tm_sh_up_s, tm_sh_down_s;
+    int ws_gu, ws_d, ws_sh_gu, ws_sh_d;  // scale maps valid (else scales are read directly)
     int T, k, H, I;
     int max_active;               // host-side upper bound of n_active (grid sizing)
     // routed experts
@@ -73,26 +92,27 @@ struct GemvArgs {
     const int32_t* active;
     const int32_t* n_active;
     const float* topk_w;
-    // quantised activations
-    const int16_t* xq;
-    const float* xsc;
-    const int* xsum;
-    float* h;                     // [T*k][I] dispatch order
-    float* sh_h;                  // [T][I_sh]
-    const int16_t* hq;
-    const float* hsc;
-    const int* hsum;
-    const int16_t* sh_hq;
-    const float* sh_hsc;
-    const int* sh_hsum;
+    // quantised activations: int16 values, {scale, sum} per group (row stride *_gld groups)
+    const int16_t* xq;            // [T][H]
+    const int2* xmeta;
+    int16_t* hq;                  // [T*k][I] dispatch order
+    int2* hmeta;
+    int16_t* sh_hq;               // [T][I_sh]
+    int2* sh_hmeta;
+    int x_gld, h_gld, sh_gld;
     // outputs
     float* rows_out;              // ROWS mode: [T*k][H] unweighted, dispatch order
     float* sh_rows_out;           // ROWS mode: [T][H] gated shared rows
+    float* slot_term;             // COMBINE mode: [T*k][H] weighted, slot order
+    float* sh_term;               // COMBINE mode: [T][H] gated shared rows
+    int* col_counter;             // COMBINE mode: [H/32] zero between calls
+    int* status;                  // device status word (bounded-wait timeouts)
     const uint16_t* residual;     // COMBINE mode
     float* y;                     // COMBINE mode: [T][H]
 };
-bool gemv_supported(int H, int I, int I_sh);
-cudaError_t launch_gateup_gemv(const GemvArgs& p, int num_sms, cudaStream_t st);
+// Builds the tensor maps of GemvArgs from its weight pointers; false if encoding fails.
+bool gemv_tensor_maps(GemvArgs& p, int E);
+cudaError_t launch_gateup_gemv(const GemvArgs& p, cudaStream_t st);
 cudaError_t launch_down_gemv(const GemvArgs& p, bool combine, cudaStream_t st);
 
 // gemm_sm100.cu -- tensor arm (tcgen05 / TMEM grouped GEMM)

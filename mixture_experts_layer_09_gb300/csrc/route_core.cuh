@@ -1,0 +1,206 @@
+// route_core.cuh -- device pieces of stage 1 (top-k of one logit row, one warp) and stage 2
+// (per-warp histogram walk, CTA scans, bucket placement), shared by the stand-alone router and
+// dispatch kernels and by the fused decode routing kernel.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ softmax top-k
+// One warp per token with the whole logit row in registers, no shared memory, one read of the
+// row (vllm.cpp PR #481 "gate(#378): the first DEVICE run of the warp MoE router", warp-router
+// commit).  Selection is k rounds of a warp argmax with the lowest index winning a tie;
+// weights are the fp32 softmax over all E logits renormalised over the k picks; the picks are
+// written in ascending expert id.
+template <typename Tin>
+__device__ __forceinline__ float load_logit(const Tin* p);
+template <>
+__device__ __forceinline__ float load_logit<float>(const float* p) { return __ldg(p); }
+template <>
+__device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p) { return bf16_to_f32(__ldg(p)); }
+
+// VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
+// One warp selects the top-k of one logit row.  ids/w receive the row's k outputs.
+template <typename Tin, int VPT>
+__device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E, int k, int32_t* __restrict__ ids,
+                                              float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    float v[VPT];
+    bool picked[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E) {
+            float f = load_logit<Tin>(row + e);
+            v[j] = (f != f) ? -INFINITY : f;  // NaN never wins a pick
+            picked[j] = false;
+        } else {
+            v[j] = -INFINITY;
+            picked[j] = true;  // padding is never a candidate
+        }
+    }
+    // k rounds of a warp argmax: larger value first, lower expert index on a tie.
+    for (int round = 0; round < k; ++round) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int e = lane + 32 * j;
+            if (!picked[j] && (v[j] > bv || (v[j] == bv && e < bi))) {
+                bv = v[j];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi != 0x7fffffff && (bi & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j)
+                if (bi == lane + 32 * j) picked[j] = true;
+        }
+    }
+    // softmax over all E logits in fp32, renormalised over the picks
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j)
+        if (lane + 32 * j < E) m = fmaxf(m, v[j]);
+    m = warp_max(m);
+    float p[VPT];
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        p[j] = (lane + 32 * j < E && m > -INFINITY) ? expf(v[j] - m) : 0.f;
+        z += p[j];
+    }
+    z = warp_sum(z);
+    float psel = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        p[j] = (z > 0.f) ? p[j] / z : 0.f;
+        if (picked[j] && lane + 32 * j < E) psel += p[j];
+    }
+    psel = warp_sum(psel);
+    // write the picks in ascending expert id: (j, lane) order
+    int base = 0;
+    const unsigned lt = lanemask_lt();
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const bool mine = picked[j] && (lane + 32 * j < E);
+        const unsigned b = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+            const int pos = base + __popc(b & lt);
+            if (pos < k) {
+                ids[pos] = lane + 32 * j;
+                // denominator guard: a row with no finite logit spreads the weight evenly
+                w[pos] = (psel > 0.f) ? p[j] / psel : 1.f / k;
+            }
+        }
+        base += __popc(b);
+    }
+}
+
+
+// ------------------------------------------------------------------ dispatch pieces
+// Walk a warp's slot run 32 at a time.  mode 0: count into hist; mode 1: scatter using hist
+// as the running base (hist must hold the warp's starting position per expert).
+__device__ __forceinline__ void warp_walk(const int32_t* ids, int begin, int end, int E,
+                                          int* hist, int mode, int32_t* __restrict__ perm,
+                                          int32_t* __restrict__ inv, int* status) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = lanemask_lt();
+    for (int base = begin; base < end; base += 32) {
+        const int a = base + lane;
+        int id = -1;
+        if (a < end) {
+            id = __ldcg(ids + a);  // coherent: the ids may come from the same kernel
+            if (id < 0 || id >= E) {
+                if (mode == 0) record_status(status, MOE_ERR_DEVICE_INDEX, a, id);
+                id = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, id);
+        const int leader = __ffs(peers) - 1;
+        if (mode == 0) {
+            if (id >= 0 && lane == leader) hist[id] += __popc(peers);
+        } else {
+            int pos = -1;
+            if (id >= 0) pos = hist[id] + __popc(peers & lt);
+            __syncwarp();
+            if (id >= 0 && lane == leader) hist[id] += __popc(peers);
+            if (a < end) {
+                if (id >= 0) perm[pos] = a;
+                inv[a] = pos;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Exclusive scan of v over threads 0..255 (v = 0 for threads >= n); returns the prefix and
+// writes the total to *total.  Uses scratch[8 + 1].
+__device__ __forceinline__ int cta_exclusive_scan_256(int v, int* scratch, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (threadIdx.x < 256 && lane == 31) scratch[w] = incl;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int i = 0; i < 8; ++i) {
+            const int tmp = scratch[i];
+            scratch[i] = run;
+            run += tmp;
+        }
+        scratch[8] = run;
+    }
+    __syncthreads();
+    const int res = (threadIdx.x < 256) ? scratch[w] + incl - v : 0;
+    *total = scratch[8];
+    __syncthreads();
+    return res;
+}
+
+// After per-(warp or CTA) counts are known: counts, offsets, active list, and turns the
+// count table cnt[rows][E] into starting positions.  Needs blockDim.x >= 256.
+__device__ inline void finalize_plan(int* cnt, int rows, int E, int n, int32_t* counts, int32_t* offsets,
+                              int32_t* active, int32_t* n_active, int* scratch) {
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) {
+        for (int r = 0; r < rows; ++r) {
+            const int tmp = cnt[static_cast<size_t>(r) * E + e];
+            cnt[static_cast<size_t>(r) * E + e] = total;
+            total += tmp;
+        }
+    }
+    int sum;
+    const int off = cta_exclusive_scan_256(e < E ? total : 0, scratch, &sum);
+    const int flag = (e < E && total > 0) ? 1 : 0;
+    int nact;
+    const int apos = cta_exclusive_scan_256(flag, scratch, &nact);
+    if (e < E) {
+        offsets[e] = off;
+        if (counts) counts[e] = total;
+        for (int r = 0; r < rows; ++r) cnt[static_cast<size_t>(r) * E + e] += off;
+        if (flag) active[apos] = e;
+    }
+    if (threadIdx.x == 0) {
+        offsets[E] = sum;
+        *n_active = nact;
+    }
+    (void)n;
+}
+
+}  // namespace moe

@@ -13,15 +13,32 @@
 // over the k picks; the picks are written in ascending expert id.
 #include "common.cuh"
 #include "internal.h"
+#include "quant.cuh"
+#include "route_core.cuh"
 
 namespace moe {
 
 // ------------------------------------------------------------------ logits, decode GEMV
 // One CTA (128 threads) per router row; thread c covers 16-byte chunks c, c+128, ... of H.
+// CTAs past the router rows quantise x for the GEMV arm (4 warps, one (token, group of 32)
+// each) when xq != nullptr, so that step costs no launch of its own.
 template <int TB>
 __global__ void __launch_bounds__(128) router_logits_gemv_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
-    int T, int H, int E, int ld, float* __restrict__ logits) {
+    int T, int H, int E, int ld, float* __restrict__ logits, int nrows, int16_t* __restrict__ xq,
+    int2* __restrict__ xmeta, int x_gld) {
+    pdl_wait();
+    pdl_trigger();
+    if (static_cast<int>(blockIdx.x) >= nrows) {
+        const int ng = H / 32, lane = threadIdx.x & 31;
+        const int gw = (blockIdx.x - nrows) * 4 + (threadIdx.x >> 5);
+        if (gw >= T * ng) return;
+        const int t = gw / ng, grp = gw % ng;
+        const float v = bf16_to_f32(x[static_cast<size_t>(t) * H + grp * 32 + lane]);
+        quantize_group(v, lane, xq + static_cast<size_t>(t) * act_row(H), grp, kSliceX,
+                       xmeta + static_cast<size_t>(t) * x_gld + grp);
+        return;
+    }
     const int row = blockIdx.x;  // 0..E-1 router rows, E = gate row
     const uint16_t* w = (row < E) ? W_r + static_cast<size_t>(row) * H : g;
     const int nch = H / 8;
@@ -74,6 +91,8 @@ constexpr int RG_BT = 64, RG_BR = 32, RG_BK = 32;
 __global__ void __launch_bounds__(256) router_logits_gemm_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
     int T, int H, int E, int nrows, int ld, float* __restrict__ logits) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ float xs[RG_BK][RG_BT + 4];
     __shared__ float ws[RG_BK][RG_BR + 4];
     const int t0 = blockIdx.x * RG_BT, r0 = blockIdx.y * RG_BR;
@@ -135,120 +154,44 @@ __global__ void __launch_bounds__(256) router_logits_gemm_kernel(
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
-                                 int E, float* logits, cudaStream_t st) {
+                                 int E, float* logits, cudaStream_t st, int16_t* xq, int2* xmeta, int x_gld) {
+    if (x_gld == 0) x_gld = H / 32;
     if (T == 0) return cudaSuccess;
     const int nrows = E + (g ? 1 : 0);
     const int ld = nrows;
     if (T <= 32) {
-        KernelScope ks_("router_logits_gemv", st);
+        const int qctas = xq ? (T * (H / 32) + 3) / 4 : 0;
+        KernelScope ks_(xq ? "router_logits_gemv+quant_x" : "router_logits_gemv", st);
         if (T <= 4)
-            router_logits_gemv_kernel<4><<<nrows, 128, 0, st>>>(x, W_r, g, T, H, E, ld, logits);
-        else
-            router_logits_gemv_kernel<8><<<nrows, 128, 0, st>>>(x, W_r, g, T, H, E, ld, logits);
-    } else {
+            return launch_pdl(router_logits_gemv_kernel<4>, dim3(nrows + qctas), dim3(128), 0, st, x, W_r, g, T, H, E,
+                              ld, logits, nrows, xq, xmeta, x_gld);
+        return launch_pdl(router_logits_gemv_kernel<8>, dim3(nrows + qctas), dim3(128), 0, st, x, W_r, g, T, H, E, ld,
+                          logits, nrows, xq, xmeta, x_gld);
+    }
+    cudaError_t e;
+    {
         KernelScope ks_("router_logits_gemm", st);
         const dim3 grid((T + RG_BT - 1) / RG_BT, (nrows + RG_BR - 1) / RG_BR);
-        router_logits_gemm_kernel<<<grid, 256, 0, st>>>(x, W_r, g, T, H, E, nrows, ld, logits);
+        e = launch_pdl(router_logits_gemm_kernel, grid, dim3(256), 0, st, x, W_r, g, T, H, E, nrows, ld, logits);
     }
-    return cudaGetLastError();
+    if (e != cudaSuccess || !xq) return e;
+    QuantArgs q;
+    q.src0 = x; q.src0_bf16 = 1; q.rows0 = T; q.K0 = H; q.q0 = xq; q.meta0 = xmeta; q.gld0 = x_gld;
+    return launch_quantize(q, st);
 }
 
 // ------------------------------------------------------------------ softmax top-k
-template <typename Tin>
-__device__ __forceinline__ float load_logit(const Tin* p);
-template <>
-__device__ __forceinline__ float load_logit<float>(const float* p) { return __ldg(p); }
-template <>
-__device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p) { return bf16_to_f32(__ldg(p)); }
-
 // VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
 template <typename Tin, int VPT>
-__global__ void __launch_bounds__(256) router_topk_warp_kernel(
-    const Tin* __restrict__ logits, int ld, int T, int E, int k,
-    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w) {
-    const int lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(256) router_topk_warp_kernel(const Tin* __restrict__ logits, int ld, int T, int E,
+                                                               int k, int32_t* __restrict__ topk_ids,
+                                                               float* __restrict__ topk_w) {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    const Tin* row = logits + static_cast<size_t>(t) * ld;
-    float v[VPT];
-    bool picked[VPT];
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const int e = lane + 32 * j;
-        if (e < E) {
-            float f = load_logit<Tin>(row + e);
-            v[j] = (f != f) ? -INFINITY : f;  // NaN never wins a pick
-            picked[j] = false;
-        } else {
-            v[j] = -INFINITY;
-            picked[j] = true;  // padding is never a candidate
-        }
-    }
-    // k rounds of a warp argmax: larger value first, lower expert index on a tie.
-    for (int round = 0; round < k; ++round) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int e = lane + 32 * j;
-            if (!picked[j] && (v[j] > bv || (v[j] == bv && e < bi))) {
-                bv = v[j];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if (bi != 0x7fffffff && (bi & 31) == lane) {
-#pragma unroll
-            for (int j = 0; j < VPT; ++j)
-                if (bi == lane + 32 * j) picked[j] = true;
-        }
-    }
-    // softmax over all E logits in fp32, renormalised over the picks
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-        if (lane + 32 * j < E) m = fmaxf(m, v[j]);
-    m = warp_max(m);
-    float p[VPT];
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        p[j] = (lane + 32 * j < E && m > -INFINITY) ? expf(v[j] - m) : 0.f;
-        z += p[j];
-    }
-    z = warp_sum(z);
-    float psel = 0.f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        p[j] = (z > 0.f) ? p[j] / z : 0.f;
-        if (picked[j] && lane + 32 * j < E) psel += p[j];
-    }
-    psel = warp_sum(psel);
-    // write the picks in ascending expert id: (j, lane) order
-    int base = 0;
-    const unsigned lt = lanemask_lt();
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        const bool mine = picked[j] && (lane + 32 * j < E);
-        const unsigned b = __ballot_sync(0xffffffffu, mine);
-        if (mine) {
-            const int pos = base + __popc(b & lt);
-            if (pos < k) {
-                topk_ids[static_cast<size_t>(t) * k + pos] = lane + 32 * j;
-                // denominator guard: a row with no finite logit spreads the weight evenly
-                topk_w[static_cast<size_t>(t) * k + pos] = (psel > 0.f) ? p[j] / psel : 1.f / k;
-            }
-        }
-        base += __popc(b);
-    }
+    topk_warp_row<Tin, VPT>(logits + static_cast<size_t>(t) * ld, E, k, topk_ids + static_cast<size_t>(t) * k,
+                            topk_w + static_cast<size_t>(t) * k);
 }
 
 template <typename Tin>
@@ -258,17 +201,19 @@ static cudaError_t launch_topk_t(const Tin* logits, int ld, int T, int E, int k,
     const dim3 grid((T + 7) / 8), block(256);
     KernelScope ks_("router_topk", st);
     switch (vpt) {
-        case 1: router_topk_warp_kernel<Tin, 1><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 2: router_topk_warp_kernel<Tin, 2><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 3: router_topk_warp_kernel<Tin, 3><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 4: router_topk_warp_kernel<Tin, 4><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 5: router_topk_warp_kernel<Tin, 5><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 6: router_topk_warp_kernel<Tin, 6><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 7: router_topk_warp_kernel<Tin, 7><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
-        case 8: router_topk_warp_kernel<Tin, 8><<<grid, block, 0, st>>>(logits, ld, T, E, k, ids, w); break;
+#define MOE_TOPK_CASE(V) \
+    case V: return launch_pdl(router_topk_warp_kernel<Tin, V>, grid, block, 0, st, logits, ld, T, E, k, ids, w);
+        MOE_TOPK_CASE(1)
+        MOE_TOPK_CASE(2)
+        MOE_TOPK_CASE(3)
+        MOE_TOPK_CASE(4)
+        MOE_TOPK_CASE(5)
+        MOE_TOPK_CASE(6)
+        MOE_TOPK_CASE(7)
+        MOE_TOPK_CASE(8)
+#undef MOE_TOPK_CASE
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
