@@ -200,13 +200,7 @@ def run_ours(args, rank, world):
         if dist is not None:
             dist.barrier()
         n0 = moe.moe_launch_count()
-        clocks = Clocks(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out"))
-                                     else ".", f"clocks_bench_r{rank}_T{Tb}.csv"), local)
-        if full:
-            clocks.start()
         dt = time_loop(torch, step, steps, warmup)
-        if full:
-            out["clocks"] = clocks.stop()
         out["launches_per_step"] = (moe.moe_launch_count() - n0) / (steps + warmup)
         if dist is not None:
             t = torch.tensor([dt], device="cuda")
@@ -266,6 +260,11 @@ def run_ours(args, rank, world):
             out["d2h"] = Tb * H * 4
         return out
 
+    # SM clocks are sampled (nvidia-smi, 200 ms) over the whole measurement phase, which
+    # contains the timed region: a region of a few ms alone would fall between two samples.
+    clocks = Clocks(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+                                 f"clocks_bench_r{rank}.csv"), local)
+    clocks.start()
     main = measure(T, args.steps, args.warmup, full=True)
     sweep = {}
     for Tb in SWEEP_T:
@@ -276,6 +275,7 @@ def run_ours(args, rank, world):
                             "plain_us": 1e6 * r["plain_s"] / max(10, args.steps // 2),
                             "graph_us": 1e6 * r["graph_s"] / max(10, args.steps // 2)}
 
+    main["clocks"] = clocks.stop()
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()

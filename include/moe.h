@@ -109,10 +109,13 @@ MOE_API const char* moe_status_string(int status);
 MOE_API const char* moe_version(void);
 
 /* Router logits (stage 1, its GEMV/GEMM: one dot product per expert row and,
- * when g != NULL, one more row for the shared-expert gate "landing past the
- * router's logits", daScript PR #3988 decode span commit).
+ * when g != NULL, the shared-expert gate as one extra row whose logit is stored
+ * after the E router logits, daScript PR #3988 decode span commit).
  *   x       bf16 [T][H]        W_r bf16 [E][H]        g bf16 [H] or NULL
  *   logits  fp32 [T][E + (g != NULL)], fp32 accumulation of bf16 products.
+ * T <= 32 runs a GEMV; larger T runs a tcgen05 GEMM when H % 64 == 0,
+ * E <= 256 and x, W_r, g are 16-byte aligned (else a tiled fp32 GEMM).  The tensor-core kernel's bounded waits
+ * cannot report a timeout through this call (it has no workspace status word).
  * T = 0 is a no-op. */
 MOE_API int moe_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
                       int T, int H, int E, float* logits, moe_stream_t stream);

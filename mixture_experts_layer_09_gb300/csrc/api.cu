@@ -421,7 +421,8 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
         carve_gemv(c, T, k, W->H, W->I, I_sh, b);
         // decode batches: 4 launches -- logits (+ x quantisation), top-k + dispatch, gate/up, down + combine
         const bool fused_routing = T <= 32;
-        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H)) != cudaSuccess)
+        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H), status) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
         if (fused_routing) {
             if (launch_topk_dispatch(r.logits, ld, T, W->E, k, ids, w, r.counts, r.offsets, r.perm, r.inv, r.active,
@@ -435,7 +436,8 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
         }
         return run_gemv(mc, b, true, st);
     }
-    if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active, r.disp_scratch,
                         status, st) != cudaSuccess)

@@ -18,14 +18,16 @@
 // top-k weight in slot order (the tensor arm's combine feed), or the shared expert's rows
 // scaled by sigmoid of its gate logit.
 //
-// Roles in a CTA of 192 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
-// memory and issues the MMAs (one thread), warps 2-5 dequantise A and then run the epilogue.
+// Roles in a CTA of 320 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
+// memory and issues the MMAs (one thread), warps 2-9 dequantise A (two threads per weight
+// row) and then run the epilogue (each warp one TMEM lane quadrant and half the columns).
 // Every mbarrier wait is bounded; a wait that runs out records MOE_ERR_DEVICE_TIMEOUT in the
 // status word, stops the CTA's loops, drains its own copies and MMAs, frees its tensor
 // memory and returns.
 #include <cuda.h>
 
 #include "async.cuh"
+#include "tcgen05.cuh"
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,8 +38,10 @@ constexpr int BN = kGemmTileN;    // tokens per tile (MMA N upper bound)
 constexpr int BK = 64;            // K per pipeline stage: 128 bytes of fp16 per row
 constexpr int kTileBytesA = BM * BK * 2;
 constexpr int kTileBytesB = BN * BK * 2;
-constexpr int kStagesGU = 4;
-constexpr int kStagesDN = 6;
+constexpr int kStagesGU = 3;
+constexpr int kStagesDN = 4;
+constexpr int kDqThreads = 256;                 // dequantising / epilogue threads (warps 2..9)
+constexpr int kGemmThreads = 64 + kDqThreads;   // + TMA warp + MMA warp
 
 struct GemmK {
     CUtensorMap tm_r;     // B operand of routed tiles
@@ -72,123 +76,63 @@ struct GemmK {
 };
 
 
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// K-major operand tile in the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes
-// apart, 16-byte chunk c of row r stored at chunk c ^ (r & 7).
-__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
-    d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: next 8 rows
-    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
-    d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
-    return d;
-}
-
-// kind::f16 instruction descriptor: fp16 A and B, fp32 D, both K-major, M = 128.
-__device__ __forceinline__ uint32_t idesc_f16_m128(int n) {
-    return (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-           (static_cast<uint32_t>(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 8 nibbles (columns 0..7 at bits 4c) times one fp16 scale -> 8 fp16 in column order.
+// 8 nibbles (columns 0..7 at bits 4c) times one fp16 scale -> 8 fp16 values, stored in the
+// K order [c0 c4 c1 c5 c2 c6 c3 c7] (the activations are stored in the same order, so the
+// product over K is unchanged and no byte permute is needed).
 __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
-    const uint32_t t0 = (w & 0x000F000Fu) | 0x64006400u;          // cols 0, 4 as 1024 + n
-    const uint32_t t1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;   // cols 1, 5
-    const uint32_t t2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;   // cols 2, 6
-    const uint32_t t3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;  // cols 3, 7
-    const uint32_t p01 = __byte_perm(t0, t1, 0x5410);
-    const uint32_t p23 = __byte_perm(t2, t3, 0x5410);
-    const uint32_t p45 = __byte_perm(t0, t1, 0x7632);
-    const uint32_t p67 = __byte_perm(t2, t3, 0x7632);
+    const uint32_t t0 = (w & 0x000F000Fu) | 0x64006400u;          // c0, c4 as 1024 + n
+    const uint32_t t1 = ((w >> 4) & 0x000F000Fu) | 0x64006400u;   // c1, c5
+    const uint32_t t2 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;   // c2, c6
+    const uint32_t t3 = ((w >> 12) & 0x000F000Fu) | 0x64006400u;  // c3, c7
     const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
     uint4 out;
     __half2 v;
-    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p01), k1032), s2);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&t0), k1032), s2);
     out.x = *reinterpret_cast<uint32_t*>(&v);
-    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p23), k1032), s2);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&t1), k1032), s2);
     out.y = *reinterpret_cast<uint32_t*>(&v);
-    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p45), k1032), s2);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&t2), k1032), s2);
     out.z = *reinterpret_cast<uint32_t*>(&v);
-    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&p67), k1032), s2);
+    v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&t3), k1032), s2);
     out.w = *reinterpret_cast<uint32_t*>(&v);
     return out;
 }
 
-struct RawK {  // one K-step of one weight row: 32 bytes of nibbles + two fp16 scales
-    uint4 q0, q1;
-    uint32_t s;
+// Position of column c (0..7) of an 8-column group in that K order.
+__host__ __device__ constexpr inline int kperm8(int c) { return (c & 3) * 2 + (c >> 2); }
+
+// One K-step (64 columns) of half a weight row: 16 bytes of nibbles and the group's scale.
+struct RawK {
+    uint4 q;
+    uint16_t s;
 };
 
-__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, bool valid) {
+__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, int half, bool valid) {
     RawK r;
     if (valid) {
-        const uint4* p = reinterpret_cast<const uint4*>(qrow + kb * 32);
-        r.q0 = ldg_nc(p);
-        r.q1 = ldg_nc(p + 1);
-        r.s = __ldg(reinterpret_cast<const uint32_t*>(srow + kb * 2));
+        r.q = ldg_nc(qrow + kb * 32 + half * 16);
+        r.s = __ldg(srow + kb * 2 + half);
     } else {
-        r.q0 = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // all zero weights
-        r.q1 = r.q0;
+        r.q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // all zero weights
         r.s = 0;
     }
     return r;
 }
 
-__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, const RawK& r) {
-    const __half2 s_lo = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.s & 0xffffu)));
-    const __half2 s_hi = __half2half2(__ushort_as_half(static_cast<uint16_t>(r.s >> 16)));
-    const uint32_t w[8] = {r.q0.x, r.q0.y, r.q0.z, r.q0.w, r.q1.x, r.q1.y, r.q1.z, r.q1.w};
+// Writes chunks half*4 .. half*4+3 of `row` into a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int half, const RawK& r) {
+    const __half2 s2 = __half2half2(__ushort_as_half(r.s));
+    const uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
     uint8_t* rowp = tile + row * 128;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const uint4 v = dequant8(w[m], m < 4 ? s_lo : s_hi);
-        *reinterpret_cast<uint4*>(rowp + ((m ^ (row & 7)) << 4)) = v;
+    for (int j = 0; j < 4; ++j) {
+        const int c = half * 4 + j;
+        *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = dequant8(w[j], s2);
     }
 }
 
 template <int MODE>  // 0 = gate+up (two accumulators, SwiGLU epilogue), 1 = down
-__global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant__ GemmK p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmK p) {
     pdl_wait();
     pdl_trigger();
     constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
@@ -230,11 +174,13 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
     uint64_t* drain = accum + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* row_slot = const_cast<int*>(abort_flag) + 1;           // [BN] down: slot of each tile row
+    float* row_w = reinterpret_cast<float*>(row_slot + BN);     // [BN] down: its weight / shared gate
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_a + s, 128);
+            mbar_init(full_a + s, kDqThreads);
             mbar_init(full_b + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -310,9 +256,10 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
             }
         }
     } else {
-        // ---------------- A producers, then the epilogue (warps 2..5, 128 threads)
-        const int pr = threadIdx.x - 64;  // weight row within the block
-        const int wrow = mblk * BM + pr;  // weight row within the matrix
+        // ---------------- A producers (8 warps: two threads per weight row), then the epilogue
+        const int dt = threadIdx.x - 64;
+        const int pr = dt >> 1, half = dt & 1;  // weight row within the block, half of its K-step
+        const int wrow = mblk * BM + pr;        // weight row within the matrix
         const bool valid = wrow < M;
         const size_t grow = shared ? static_cast<size_t>(wrow) : static_cast<size_t>(e) * M + wrow;
         const uint8_t* qa = (shared ? p.qa_s : p.qa_r) + grow * (K / 2);
@@ -323,74 +270,85 @@ __global__ void __launch_bounds__(192, 1) moe_gemm_kernel(const __grid_constant_
             qb = (shared ? p.qb_s : p.qb_r) + grow * (K / 2);
             sb = (shared ? p.sb_s : p.sb_r) + grow * (K / 32);
         }
-        RawK ra = load_raw(qa, sa, 0, valid), rb{};
-        if (MODE == 0) rb = load_raw(qb, sb, 0, valid);
+        if (MODE == 1) {
+            // the epilogue's per-row data, loaded now so it is not on the epilogue's path
+            if (dt < nrows) {
+                const int r = row0 + dt;
+                if (shared) {
+                    float gate = 1.f;
+                    if (p.sh_gate_logit) gate = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
+                    row_slot[dt] = r;
+                    row_w[dt] = gate;
+                } else if (p.out_mode == 1) {  // weighted slot rows; rows mode needs no table
+                    const int a = __ldg(p.perm + r);
+                    row_slot[dt] = a;
+                    row_w[dt] = __ldg(p.topk_w + a);
+                }
+            }
+        }
+        RawK ra = load_raw(qa, sa, 0, half, valid), rb{};
+        if (MODE == 0) rb = load_raw(qb, sb, 0, half, valid);
         bool ok = true;
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
             RawK na{}, nb{};
             if (kb + 1 < nk) {
-                na = load_raw(qa, sa, kb + 1, valid);
-                if (MODE == 0) nb = load_raw(qb, sb, kb + 1, valid);
+                na = load_raw(qa, sa, kb + 1, half, valid);
+                if (MODE == 0) nb = load_raw(qb, sb, kb + 1, half, valid);
             }
             if (kb >= S && !mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4)) {
                 ok = false;
                 break;
             }
-            store_dequant(stage_a(s, 0), pr, ra);
-            if (MODE == 0) store_dequant(stage_a(s, 1), pr, rb);
+            store_dequant(stage_a(s, 0), pr, half, ra);
+            if (MODE == 0) store_dequant(stage_a(s, 1), pr, half, rb);
             fence_proxy_async_smem();
             mbar_arrive(full_a + s);
             ra = na;
             if (MODE == 0) rb = nb;
         }
+        named_barrier(2, kDqThreads);  // row_slot / row_w visible to every epilogue thread
         // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp)
         bool go = __all_sync(0xffffffffu, ok);
         if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5));
         if (go) {
             tc_fence_after();
-            const int q = warp & 3;               // tensor-memory lane quadrant of this warp
-            const int m = q * 32 + lane;          // accumulator row = weight row in the block
-            const int n_out = mblk * BM + m;      // output feature
+            const int q = warp & 3;                 // tensor-memory lane quadrant of this warp
+            const int m = q * 32 + lane;            // accumulator row = weight row in the block
+            const int n_out = mblk * BM + m;        // output feature
+            const int ch = (warp - 2) >> 2;         // column half handled by this warp
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            for (int c0 = 0; c0 < nrows; c0 += 16) {
+            const int cbeg = ch * (BN / 2), cend = min(nrows, cbeg + BN / 2);
+            for (int c0 = cbeg; c0 < cend; c0 += 16) {
                 float d0[16];
                 tmem_ld16(tbase + c0, d0);
                 if (MODE == 0) {
                     float d1[16];
                     tmem_ld16(tbase + BN + c0, d1);
                     uint16_t* hout = shared ? p.h_s : p.h_r;
+                    const int pos = (n_out & ~7) + kperm8(n_out & 7);  // K order of the down GEMM
                     if (n_out < M) {
 #pragma unroll
                         for (int cc = 0; cc < 16; ++cc) {
                             const int c = c0 + cc;
-                            if (c < nrows) {
+                            if (c < cend) {
                                 const float g = d0[cc], u = d1[cc];
                                 const float h = g / (1.f + expf(-g)) * u;
-                                hout[static_cast<size_t>(row0 + c) * M + n_out] = __half_as_ushort(__float2half_rn(h));
+                                hout[static_cast<size_t>(row0 + c) * M + pos] = __half_as_ushort(__float2half_rn(h));
                             }
                         }
                     }
-                } else {
-                    if (n_out < M) {
+                } else if (n_out < M) {
 #pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) {
-                            const int c = c0 + cc;
-                            if (c >= nrows) continue;
-                            const int r = row0 + c;
-                            if (shared) {
-                                float gate = 1.f;
-                                if (p.sh_gate_logit) {
-                                    const float z = __ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld);
-                                    gate = 1.f / (1.f + expf(-z));
-                                }
-                                p.out_s[static_cast<size_t>(r) * M + n_out] = gate * d0[cc];
-                            } else if (p.out_mode == 0) {
-                                p.out_r[static_cast<size_t>(r) * M + n_out] = d0[cc];
-                            } else {
-                                const int a = __ldg(p.perm + r);
-                                p.out_r[static_cast<size_t>(a) * M + n_out] = __ldg(p.topk_w + a) * d0[cc];
-                            }
+                    for (int cc = 0; cc < 16; ++cc) {
+                        const int c = c0 + cc;
+                        if (c >= cend) continue;
+                        if (shared) {
+                            p.out_s[static_cast<size_t>(row0 + c) * M + n_out] = row_w[c] * d0[cc];
+                        } else if (p.out_mode == 0) {
+                            p.out_r[static_cast<size_t>(row0 + c) * M + n_out] = d0[cc];
+                        } else {
+                            p.out_r[static_cast<size_t>(row_slot[c]) * M + n_out] = row_w[c] * d0[cc];
                         }
                     }
                 }
@@ -432,7 +390,8 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     }
 }
 
-// x16[r] = fp16(x[perm[r] / k]) for the T*k dispatched rows, then x16[T*k + t] = fp16(x[t]).
+// x16[r] = fp16(x[perm[r] / k]) for the T*k dispatched rows, then x16[T*k + t] = fp16(x[t]);
+// each group of 8 columns is stored in the K order of the dequantised weight tiles.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int T, int k, int H,
                                                           int with_tokens, uint16_t* __restrict__ x16) {
@@ -447,13 +406,16 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
         const int t = (r < T * k) ? __ldg(perm + r) / k : r - T * k;
         const uint4 v = ldg_nc(x + static_cast<size_t>(t) * H + c * 8);
         const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+        uint16_t h[8];  // columns 0..7 as fp16
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const __half lo = __float2half_rn(__uint_as_float(in[j] << 16));
-            const __half hi = __float2half_rn(__uint_as_float(in[j] & 0xffff0000u));
-            out[j] = static_cast<uint32_t>(__half_as_ushort(lo)) | (static_cast<uint32_t>(__half_as_ushort(hi)) << 16);
+            h[2 * j] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] << 16)));
+            h[2 * j + 1] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] & 0xffff0000u)));
         }
+        // stored in the GEMM's K order [c0 c4 c1 c5 c2 c6 c3 c7]
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[j] = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 4]) << 16);
         reinterpret_cast<uint4*>(x16 + static_cast<size_t>(r) * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
@@ -475,7 +437,7 @@ template <int MODE>
 static size_t gemm_smem_bytes() {
     constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
     constexpr int NMAT = MODE == 0 ? 2 : 1;
-    return static_cast<size_t>(S) * (NMAT * kTileBytesA + kTileBytesB) + 1024 + 256;
+    return static_cast<size_t>(S) * (NMAT * kTileBytesA + kTileBytesB) + 1024 + 256 + 8 * BN;
 }
 
 template <int MODE>
@@ -549,7 +511,7 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
         const int ctas = g.ctas_r + (has_sh ? p.sh_tiles * g.mblk_s : 0);
         {
             KernelScope ks_("gemm_gateup", st);
-            err = launch_pdl(moe_gemm_kernel<0>, dim3(ctas), dim3(192), gemm_smem_bytes<0>(), st, g);
+            err = launch_pdl(moe_gemm_kernel<0>, dim3(ctas), dim3(kGemmThreads), gemm_smem_bytes<0>(), st, g);
         }
         if (err != cudaSuccess) return err;
     }
@@ -584,7 +546,7 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
         const int ctas = d.ctas_r + (has_sh ? p.sh_tiles * d.mblk_s : 0);
         {
             KernelScope ks_("gemm_down", st);
-            err = launch_pdl(moe_gemm_kernel<1>, dim3(ctas), dim3(192), gemm_smem_bytes<1>(), st, d);
+            err = launch_pdl(moe_gemm_kernel<1>, dim3(ctas), dim3(kGemmThreads), gemm_smem_bytes<1>(), st, d);
         }
         if (err != cudaSuccess) return err;
     }

@@ -97,16 +97,17 @@ __device__ __forceinline__ Nib split_nibbles(const uint4 w) {
 }
 
 // sum over the 32 columns of a chunk of nibble * activation; a = 32 int16 in dp2a order.
+// Four independent accumulators (one per 8-column word) keep the dp2a chains short.
 __device__ __forceinline__ int dot_nib(const Nib& n, const uint4 (&a)[4]) {
-    int acc = 0;
+    int acc[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        acc = __dp2a_lo(static_cast<int>(a[m].x), static_cast<int>(n.lo[m]), acc);
-        acc = __dp2a_hi(static_cast<int>(a[m].y), static_cast<int>(n.lo[m]), acc);
-        acc = __dp2a_lo(static_cast<int>(a[m].z), static_cast<int>(n.hi[m]), acc);
-        acc = __dp2a_hi(static_cast<int>(a[m].w), static_cast<int>(n.hi[m]), acc);
+        acc[m] = __dp2a_lo(static_cast<int>(a[m].x), static_cast<int>(n.lo[m]), 0);
+        acc[m] = __dp2a_hi(static_cast<int>(a[m].y), static_cast<int>(n.lo[m]), acc[m]);
+        acc[m] = __dp2a_lo(static_cast<int>(a[m].z), static_cast<int>(n.hi[m]), acc[m]);
+        acc[m] = __dp2a_hi(static_cast<int>(a[m].w), static_cast<int>(n.hi[m]), acc[m]);
     }
-    return acc;
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 __device__ __forceinline__ void load_act(const int16_t* p, uint4 (&a)[4]) {
@@ -234,6 +235,37 @@ __device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt
         if (threadIdx.x == 0) p.col_counter[cb] = 0;  // ready for the next call
     }
     named_barrier(1, kCW * 32);
+}
+
+// One full slice with staged scales for NB tokens: every chunk of the lane, no branches.
+template <int MODE, int NB>
+__device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, float (&acc)[Pipe<MODE>::TB][Pipe<MODE>::NMAT]) {
+    using P = Pipe<MODE>;
+    constexpr int NMAT = P::NMAT;
+#pragma unroll
+    for (int j = 0; j < P::CPL; ++j) {
+        const int c = ks + 8 * j;
+        Nib nw[NMAT];
+        float fs[NMAT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            nw[m] = split_nibbles(
+                *reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB + lrow * kBoxB + (c & 15) * 16));
+            fs[m] = f16_to_f32(*reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2));
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            uint4 av[4];
+            const uint4* ap = reinterpret_cast<const uint4*>(st + P::OFF_A + b * P::KC * 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
+            const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
+            const float asc = __int_as_float(amv.x);
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+        }
+    }
 }
 
 template <int MODE>
@@ -444,44 +476,54 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         }
         const bool ws = hd->shared ? ((MODE == 0) ? p.ws_sh_gu : p.ws_sh_d) : ((MODE == 0) ? p.ws_gu : p.ws_d);
         const int nch = min(P::KC, K - sl * P::KC) / 32;
+        if (ws && nch == P::KC / 32) {
+            // full slice with staged scales: branch-free, specialised on the token count
+            switch (nb) {
+                case 1: stage_dot<MODE, 1>(st, ks, lrow, acc); break;
+                case 2: stage_dot<MODE, 2>(st, ks, lrow, acc); break;
+                case 3: stage_dot<MODE, 3>(st, ks, lrow, acc); break;
+                default: stage_dot<MODE, 4>(st, ks, lrow, acc); break;
+            }
+        } else {
 #pragma unroll
-        for (int j = 0; j < P::CPL; ++j) {
-            const int c = ks + 8 * j;  // chunk within the slice
-            if (c < nch) {
-                Nib nw[NMAT];
-                float fs[NMAT];
+            for (int j = 0; j < P::CPL; ++j) {
+                const int c = ks + 8 * j;  // chunk within the slice
+                if (c < nch) {
+                    Nib nw[NMAT];
+                    float fs[NMAT];
 #pragma unroll
-                for (int m = 0; m < NMAT; ++m) {
-                    nw[m] = split_nibbles(*reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB +
-                                                                          lrow * kBoxB + (c & 15) * 16));
-                    uint16_t sb;
-                    if (ws) {
-                        sb = *reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2);
-                    } else {
-                        const uint16_t* srow;
-                        const int rows_pe = (MODE == 0) ? p.I : p.H;
-                        if (MODE == 0)
-                            srow = hd->shared ? (m ? p.sh_up_s : p.sh_gate_s) : (m ? p.up_s : p.gate_s);
-                        else
-                            srow = hd->shared ? p.sh_down_s : p.down_s;
-                        const size_t wrow = hd->shared ? static_cast<size_t>(hd->rb) * 32 + lrow
-                                                       : static_cast<size_t>(hd->e) * rows_pe + hd->rb * 32 + lrow;
-                        sb = __ldg(srow + wrow * (K / 32) + sl * P::GRP + c);
+                    for (int m = 0; m < NMAT; ++m) {
+                        nw[m] = split_nibbles(*reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB +
+                                                                              lrow * kBoxB + (c & 15) * 16));
+                        uint16_t sb;
+                        if (ws) {
+                            sb = *reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2);
+                        } else {
+                            const uint16_t* srow;
+                            const int rows_pe = (MODE == 0) ? p.I : p.H;
+                            if (MODE == 0)
+                                srow = hd->shared ? (m ? p.sh_up_s : p.sh_gate_s) : (m ? p.up_s : p.gate_s);
+                            else
+                                srow = hd->shared ? p.sh_down_s : p.down_s;
+                            const size_t wrow = hd->shared ? static_cast<size_t>(hd->rb) * 32 + lrow
+                                                           : static_cast<size_t>(hd->e) * rows_pe + hd->rb * 32 + lrow;
+                            sb = __ldg(srow + wrow * (K / 32) + sl * P::GRP + c);
+                        }
+                        fs[m] = f16_to_f32(sb);
                     }
-                    fs[m] = f16_to_f32(sb);
-                }
 #pragma unroll
-                for (int b = 0; b < TB; ++b) {
-                    if (b < nb) {
-                        uint4 av[4];
-                        const uint4* ap = reinterpret_cast<const uint4*>(st + P::OFF_A + b * P::KC * 2);
+                    for (int b = 0; b < TB; ++b) {
+                        if (b < nb) {
+                            uint4 av[4];
+                            const uint4* ap = reinterpret_cast<const uint4*>(st + P::OFF_A + b * P::KC * 2);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
-                        const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
-                        const float asc = __int_as_float(amv.x);
+                            for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
+                            const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
+                            const float asc = __int_as_float(amv.x);
 #pragma unroll
-                        for (int m = 0; m < NMAT; ++m)
-                            acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+                            for (int m = 0; m < NMAT; ++m)
+                                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+                        }
                     }
                 }
             }

@@ -29,7 +29,12 @@ bool tmap_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint
 // xq/xsc/xsum (optional): also quantise x for the GEMV arm in the same launch (decode batches).
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
                                  int E, float* logits, cudaStream_t st, int16_t* xq = nullptr,
-                                 int2* xmeta = nullptr, int x_gld = 0);
+                                 int2* xmeta = nullptr, int x_gld = 0, int* status = nullptr);
+// router_tc.cu: tcgen05 logits GEMM for T > 32 (status: device timeout record, may be null)
+// (H % 64 == 0, 1 <= E <= 256, x / W_r / g 16-byte aligned)
+bool router_tc_supported(const void* x, const void* W_r, const void* g, int H, int E);
+cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H, int E,
+                                    float* logits, int* status, cudaStream_t st);
 // group row stride of the quantised activations: K/32 rounded up to a multiple of 4
 inline int act_gld(int K) { return ((K / 32) + 3) & ~3; }
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
@@ -152,7 +157,7 @@ struct GemmPlan {
     float* slot_out;              // SLOT mode [T*k][H], weighted, slot order
     float* sh_out;                // [T][H] gated shared rows
 };
-constexpr int kGemmTileN = 128;   // tokens per tile
+constexpr int kGemmTileN = 256;   // tokens per tile
 int gemm_ntile_max(int n_slots, int E);
 bool gemm_supported(int H, int I, int I_sh);
 cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st);

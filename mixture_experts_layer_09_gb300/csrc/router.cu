@@ -4,7 +4,8 @@
 // shared-expert gate vector as one more row past the router's E rows (daScript PR #3988
 // "dasLLAMA vulkan: a MoE that fits the card ...", decode span commit: the gate logit is one
 // more router GEMV row).  Decode batches (T <= 32) run a GEMV that reads every router row
-// once; larger batches run a tiled fp32 GEMM.
+// once; larger batches run a tcgen05 GEMM (router_tc.cu), or a tiled fp32 GEMM where H is not a
+// multiple of 64 or E is above 256.
 //
 // Top-k: one warp per token with the whole logit row in registers, no shared memory, no
 // block barrier and one read of the row (vllm.cpp PR #481 "gate(#378): the first DEVICE run
@@ -154,7 +155,8 @@ __global__ void __launch_bounds__(256) router_logits_gemm_kernel(
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
-                                 int E, float* logits, cudaStream_t st, int16_t* xq, int2* xmeta, int x_gld) {
+                                 int E, float* logits, cudaStream_t st, int16_t* xq, int2* xmeta, int x_gld,
+                                 int* status) {
     if (x_gld == 0) x_gld = H / 32;
     if (T == 0) return cudaSuccess;
     const int nrows = E + (g ? 1 : 0);
@@ -169,7 +171,9 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const u
                           logits, nrows, xq, xmeta, x_gld);
     }
     cudaError_t e;
-    {
+    if (router_tc_supported(x, W_r, g, H, E)) {
+        e = launch_router_logits_tc(x, W_r, g, T, H, E, logits, status, st);
+    } else {
         KernelScope ks_("router_logits_gemm", st);
         const dim3 grid((T + RG_BT - 1) / RG_BT, (nrows + RG_BR - 1) / RG_BR);
         e = launch_pdl(router_logits_gemm_kernel, grid, dim3(256), 0, st, x, W_r, g, T, H, E, nrows, ld, logits);

@@ -74,7 +74,10 @@ def test_topk_strided_rows_and_nan(moe):
 
 
 @pytest.mark.parametrize("T,E,H,with_g", [(1, 128, 2048, False), (16, 128, 2048, False), (8, 256, 6144, False),
-                                          (512, 60, 2048, True), (100, 8, 256, True), (4096, 60, 2048, True)])
+                                          (512, 60, 2048, True), (100, 8, 256, True), (4096, 60, 2048, True),
+                                          # tensor-core path: second MMA column chunk (E + 1 = 257), E = 1,
+                                          # and the fp32 GEMM fallback (H not a multiple of 64)
+                                          (300, 256, 1024, True), (200, 1, 128, True), (40, 128, 2080, False)])
 def test_router_logits(moe, T, E, H, with_g):
     import torch
     x = gen.draw_x(3, T, H)
