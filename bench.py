@@ -131,6 +131,86 @@ def run_reference(args, rank):
 
 # ----------------------------------------------------------------------------- our arm
 
+# DRAM traffic of a kernel from an ncu capture, valid while the sources it was built from are
+# unchanged: profiles/dram_traffic.txt holds lines "kernel bytes_per_unit unit sha256 note", the
+# hash taken over KERNEL_SOURCES by source_hash(); the GEMV kernels' unit is one distinct expert
+# streamed by the launch, so a launch's traffic is bytes_per_unit x its distinct experts.
+KERNEL_SOURCES = {
+    "gateup_gemv": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "internal.h"),
+    "down_gemv_combine": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "internal.h"),
+    "gemm_gateup": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "internal.h"),
+    "gemm_down": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "internal.h"),
+}
+
+
+def source_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, ()):
+        with open(os.path.join(ROOT, "mixture_experts_layer_09_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(kernel, units):
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if kernel not in KERNEL_SOURCES or not os.path.exists(p):
+        return None
+    for ln in open(p):
+        parts = ln.split(None, 4)
+        if len(parts) >= 4 and not ln.startswith("#") and parts[0] == kernel and parts[3] == source_hash(kernel):
+            per = float(parts[1])
+            scale = units if parts[2] == "expert" else 1.0
+            return {"bytes": per * scale, "note": (parts[4].strip() if len(parts) > 4 else "")}
+    return None
+
+
+PREFILL = dict(name="qwen15_moe_a2.7b_prefill_layer", H=2048, I=1408, E=60, k=4, I_sh=5632, T=(4096, 512))
+
+
+def measure_prefill(torch, moe, args):
+    """Prefill layer (grouped GEMM arm, tensor-core bound): us/layer, tokens/s and the fraction
+    of the bf16 dense peak that the layer and its two GEMMs reach."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    P = PREFILL
+    _, tc, src = peaks()
+    res = {"workload": f"{P['name']} H={P['H']} I={P['I']} E={P['E']} k={P['k']} I_sh={P['I_sh']}"}
+    reps = 2  # 2 x 300 MB of int4 weights cycled: more than L2
+    layers = [upload(torch, moe, gen.Workload("p", max(P["T"]), P["H"], P["I"], P["E"], P["k"], I_sh=P["I_sh"]),
+                     50 + r) for r in range(reps)]
+    H, I, k, I_sh = P["H"], P["I"], P["k"], P["I_sh"]
+    for T in P["T"]:
+        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+        xs = [to(gen.draw_x(900 + i, T, H)) for i in range(4)]
+        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+
+        def step(i):
+            layers[i % reps].forward(xs[i % 4], None, y=y)
+
+        steps = max(10, args.steps // 2)
+        dt = time_loop(torch, step, steps, args.warmup)
+        moe.moe_profile_enable(True)
+        time_loop(torch, step, steps, 0)
+        kern = moe.moe_profile_read()
+        moe.moe_profile_enable(False)
+        us = 1e6 * dt / steps
+        fl = {"gemm_gateup": 2.0 * (T * k * H * 2 * I + T * H * 2 * I_sh),
+              "gemm_down": 2.0 * (T * k * I * H + T * I_sh * H)}
+        layer_flops = sum(fl.values()) + 2.0 * T * H * (P["E"] + 1)
+        kus = {n: 1e3 * v[0] / steps for n, v in kern.items()}
+        gem = {n: {"us": kus[n], "tflops": fl[n] / (kus[n] * 1e-6) / 1e12,
+                   "frac": fl[n] / (kus[n] * 1e-6) / 1e12 / tc} for n in fl if n in kus}
+        res[f"T={T}"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+                         "layer_tflops": layer_flops / (us * 1e-6) / 1e12,
+                         "layer_tc_frac": layer_flops / (us * 1e-6) / 1e12 / tc,
+                         "gemm": gem, "kernels_us": kus}
+    res["peak_tflops"] = tc
+    res["peak_source"] = f"bf16 dense burst, {src} (the MMAs take fp16 operands: same dense rate)"
+    del layers
+    torch.cuda.empty_cache()
+    return res
+
+
 def upload_layer(torch, moe, inp):
     def dev(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
@@ -275,6 +355,7 @@ def run_ours(args, rank, world):
                             "plain_us": 1e6 * r["plain_s"] / max(10, args.steps // 2),
                             "graph_us": 1e6 * r["graph_s"] / max(10, args.steps // 2)}
 
+    prefill = measure_prefill(torch, moe, args) if not args.no_prefill else None
     main["clocks"] = clocks.stop()
     if rank != 0:
         if dist is not None:
@@ -297,6 +378,7 @@ def run_ours(args, rank, world):
         + T * H * 2 + T * H * 4,
     }
     ach = per_kernel_bytes.get(dom, float("nan")) / (dom_ms * 1e-3) / 1e9
+    traffic = dram_traffic(dom, nd)
     layer_bytes = nd * bpe + E * H * 2 + T * H * (2 + 2 + 4)
     layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
     line = {
@@ -314,27 +396,35 @@ def run_ours(args, rank, world):
                    "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm,
                    "sweep": sweep},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                     "frac": ach / hbm, "peak_source": src, "traffic": None,
-                     "kernel_us": dom_ms * 1e3},
+                     "frac": ach / hbm, "peak_source": src,
+                     "traffic": traffic["bytes"] if traffic else None,
+                     "traffic_note": traffic["note"] if traffic else "no ncu capture of this kernel's current source",
+                     "algorithmic_bytes": per_kernel_bytes.get(dom), "kernel_us": dom_ms * 1e3},
         "kernels_us_per_step": {n: 1e3 * v[0] / steps for n, v in kern.items()},
         "gpu_launches": int(round(main["launches_per_step"] * steps)),
+        "prefill": prefill,
         "clocks": main.get("clocks"),
         "e2e": {"value": world * T * steps / main["e2e_s"], "unit": "tokens/s",
                 "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
     }
     if not args.no_cpu_baseline:
+        # the oracle as it stands, one host thread, on whole batches of the same workload (one
+        # drawn layer, a fresh token batch each time) until about 10 s of CPU work is done
+        import dataclasses
+
         import oracle
         oracle.build()
-        wl = gen.Workload(WORKLOAD["name"], T, H, I, E, k)
-        inp = gen.draw_layer(wl)
-        n_tok = 4
-        mask = np.zeros(T, dtype=np.uint8)
-        mask[:n_tok] = 1
-        t0 = time.perf_counter()
-        oracle.layer_forward(inp, token_mask=mask)
-        dt = time.perf_counter() - t0
+        base = gen.draw_layer(gen.Workload(WORKLOAD["name"], T, H, I, E, k))
+        n_tok, dt, b = 0, 0.0, 0
+        while b == 0 or dt < 10.0:
+            inp = dataclasses.replace(base, x=gen.draw_x(500 + b, T, H)) if b else base
+            t0 = time.perf_counter()
+            oracle.layer_forward(inp)
+            dt += time.perf_counter() - t0
+            n_tok += T
+            b += 1
         line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{n_tok} tokens of the T={T} batch (routing for all {T})"}
+                                "sample": f"{b} batches of T={T} tokens ({n_tok} tokens, {dt:.1f} s)"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -347,6 +437,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-layer section")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
