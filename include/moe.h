@@ -195,10 +195,12 @@ MOE_API int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const
                       float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Clears the head of a workspace (its first 4096 bytes: the device status word and the
- * down projection's column counters) on `stream`.  A workspace must start with a zero head:
- * call this once on a new workspace, or allocate it zero-filled.  The calls above leave the
- * head zero again (except a recorded status). */
+/* Clears the head of a workspace (its first 4096 bytes: the device status word, the GEMV
+ * arm's task claim counters and the down projection's column counters) on `stream`.  A
+ * workspace must start with a zero head: call this once on a new workspace, or allocate it
+ * zero-filled.  The calls above leave the head zero again (except a recorded status); after
+ * a call that recorded MOE_ERR_DEVICE_TIMEOUT the counters may not be zero, so call this
+ * again before reusing the workspace. */
 MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronises `stream`, copies the device status word of a workspace used by

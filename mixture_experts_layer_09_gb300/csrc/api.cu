@@ -209,6 +209,7 @@ int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
     }
     p.offsets = c.offsets; p.perm = c.perm; p.active = c.active; p.n_active = c.n_active; p.topk_w = c.topk_w;
     p.status = c.status;
+    p.task_counter = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + kWsTaskOffset);
     p.x_gld = act_gld(W->H); p.h_gld = act_gld(W->I); p.sh_gld = act_gld(I_sh > 0 ? I_sh : 32);
     p.xq = b.xq; p.xmeta = b.xmeta;
     p.hq = b.hq; p.hmeta = b.hmeta; p.sh_hq = b.sh_hq; p.sh_hmeta = b.sh_hmeta;

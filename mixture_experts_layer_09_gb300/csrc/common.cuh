@@ -17,10 +17,12 @@ namespace moe {
 
 constexpr int kWarp = 32;
 constexpr size_t kWsAlign = 256;
-// Head of every workspace: the device status word at offset 0 and, from kWsCounterOffset,
-// the per-column-block counters of the GEMV down projection (zero between calls).
+// Head of every workspace: the device status word at offset 0, the GEMV task claim counters
+// at kWsTaskOffset and, from kWsCounterOffset, the per-column-block counters of the GEMV down
+// projection.  The kernels leave every counter at zero when they finish.
 constexpr size_t kWsHead = 4096;
 constexpr size_t kWsCounterOffset = 1024;
+constexpr size_t kWsTaskOffset = 512;  // GEMV task claim counters (4 ints)
 constexpr int kMaxColBlocks = static_cast<int>((kWsHead - kWsCounterOffset) / sizeof(int));  // H <= 24576
 
 // Device status word layout (first 256 bytes of every workspace).

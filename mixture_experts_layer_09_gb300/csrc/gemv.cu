@@ -153,6 +153,9 @@ __device__ __forceinline__ float row_sum8(float v) {
 
 constexpr int kBoxB = 256;  // bytes of one weight TMA box row (512 K-columns)
 constexpr int kCW = 8;      // consumer warps
+// producer lanes issuing a stage's copies: weight boxes from lane 0, scale boxes, activation
+// slices and their {scale, sum} pairs from these lanes on (one copy per lane)
+constexpr int kLaneScale = 8, kLaneAct = 16, kLaneMeta = 24;
 
 template <int MODE>
 struct Pipe {
@@ -170,6 +173,7 @@ struct Pipe {
     static constexpr int STAGE = (OFF_HDR + 256 + 1023) / 1024 * 1024;
     static constexpr int STAGES = (MODE == 0) ? 4 : 3;  // two CTAs fit one SM
     static_assert(OFF_WS % 128 == 0 && OFF_A % 128 == 0 && OFF_AM % 16 == 0, "copy destinations aligned");
+    static_assert(NMAT * NBOX <= kLaneScale && TB <= 8, "one copy per producer lane");
 };
 
 struct StageHdr {
@@ -215,11 +219,14 @@ __device__ __forceinline__ void task_desc(const GemvArgs& p, int t, int n_act, i
 // MODE 1: publish `cnt` finished tasks of column block cb; the CTA that completes the block
 // sums, per token, the shared row, the slots in order and the residual, then resets the counter.
 __device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt, int n_act, int* last_flag) {
-    __threadfence();
+    // the consumers' term stores happen before thread 0's fence (barrier), and the fence orders
+    // them before the count (release); the completing CTA fences after reading the count (acquire)
     named_barrier(1, kCW * 32);
     if (threadIdx.x == 0) {
         const int expected = n_act + (p.sh_I > 0 ? 1 : 0);
+        __threadfence();
         *last_flag = (atomicAdd(p.col_counter + cb, cnt) + cnt == expected);
+        __threadfence();
     }
     named_barrier(1, kCW * 32);
     if (*last_flag) {
@@ -268,6 +275,54 @@ __device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, f
     }
 }
 
+// MODE 1: this CTA's contiguous range [first, last) of the column-block-major task list, cut at
+// equal shares of the estimated work.  A task costs about (4 + tokens) per pass of up to four
+// tokens and per K-slice; every column block holds one task of each active expert (and of the
+// shared expert), so all blocks cost the same and a cut point maps to (block, expert) by one
+// count over the experts' cost prefix.  Runs on the producer warp; n_act <= 256.
+__device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int nrb, int per_cb, int lane, int& first,
+                                               int& last) {
+    constexpr int KC = kSliceH;
+    const int nsl_r = (p.I + KC - 1) / KC;
+    long long pre[8];  // exclusive cost prefix of experts lane*8 .. lane*8+7
+    long long mine = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int a = lane * 8 + i;
+        pre[i] = mine;
+        if (a < n_act) {
+            const int e = __ldg(p.active + a);
+            const int cnt = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+            mine += static_cast<long long>(nsl_r) * (4 * ((cnt + 3) / 4) + cnt);
+        }
+    }
+    long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const long long base = incl - mine;
+    const long long routed = __shfl_sync(0xffffffffu, incl, 31);
+    long long W = routed;
+    if (p.sh_I > 0) W += static_cast<long long>((p.sh_I + KC - 1) / KC) * (4 * ((p.T + 3) / 4) + p.T);
+    if (W <= 0) W = 1;
+    const long long C = W * nrb;
+    auto cut = [&](long long pos) -> int {  // first task whose start cost is >= pos
+        if (pos >= C) return nrb * per_cb;
+        const long long cb = pos / W, rem = pos - cb * W;
+        int n = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) n += (lane * 8 + i < n_act && base + pre[i] < rem) ? 1 : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+        if (per_cb > n_act && routed < rem) ++n;  // the shared expert's task
+        return static_cast<int>(cb) * per_cb + n;
+    };
+    first = cut(C * blockIdx.x / gridDim.x);
+    last = cut(C * (blockIdx.x + 1) / gridDim.x);
+}
+
 template <int MODE>
 __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __grid_constant__ GemvArgs p) {
     using P = Pipe<MODE>;
@@ -300,11 +355,35 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         const int nsh = (p.sh_I > 0) ? ((MODE == 0) ? p.sh_I / 32 : p.H / 32) : 0;
         const int ntask = n_act * nrb + nsh;
         const int per_cb = n_act + (nsh > 0 ? 1 : 0);
-        const int len = (ntask + gridDim.x - 1) / gridDim.x;
-        const int first = blockIdx.x * len, last = min(ntask, first + len);
+        // tasks are claimed in chunks from a counter in the workspace head, the next chunk
+        // claimed while the current one streams: tasks differ in token count, so a fixed split
+        // of the list leaves some CTAs with twice the work of others
+        int* next_ctr = p.task_counter + (MODE == 0 ? 0 : 2);
+        int* done_ctr = next_ctr + 1;
+        // (the down projection with the folded combine instead walks one contiguous range per
+        // CTA, so that it leaves each column block at most once; above four tokens a task's
+        // cost depends on its token count and the ranges are cut by cost)
+        int CH = max(1, min(32, ntask / (static_cast<int>(gridDim.x) * 8)));
+        int q0, r_last = ntask;
+        if (MODE == 1) {
+            if (p.T > 4) {
+                balanced_range(p, n_act, nrb, per_cb, lane, q0, r_last);
+            } else {
+                const int len = (ntask + gridDim.x - 1) / gridDim.x;
+                q0 = min(ntask, static_cast<int>(blockIdx.x) * len);
+                r_last = min(ntask, q0 + len);
+            }
+            CH = 32;
+        } else {
+            q0 = static_cast<int>(blockIdx.x) * CH;  // first chunk: implied by the CTA index
+        }
         uint32_t it = 0;
-        for (int q0 = first; q0 < last && !*abort_flag; q0 += 32) {
-          // the warp's lanes look up the next 32 task descriptors at once
+        while (q0 < r_last && !*abort_flag) {
+          int qn = 0;
+          if (MODE != 1 && lane == 0) qn = atomicAdd(next_ctr, CH) + static_cast<int>(gridDim.x) * CH;
+          if (MODE == 1) qn = q0 + CH;
+          const int last = min(r_last, q0 + CH);
+          // the warp's lanes look up the chunk's task descriptors at once
           TaskDesc mine{};
           if (q0 + lane < last) {
               // MODE 1 walks column-block-major (block cb: experts in order, then the shared one)
@@ -315,7 +394,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
               }
               task_desc<MODE>(p, t, n_act, nrb, mine);
           }
-          const int wn = min(32, last - q0);
+          const int wn = last - q0;
           for (int j = 0; j < wn && !*abort_flag; ++j) {
             TaskDesc tk;
             tk.shared = __shfl_sync(0xffffffffu, static_cast<int>(mine.shared), j);
@@ -395,24 +474,39 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                     if (lane == 0) {
                         const uint32_t bytes = NMAT * (P::WMAT + (ws ? 32 * P::GRP * 2 : 0)) + nb * (ab + mb);
                         mbar_arrive_expect_tx(full + s, bytes);  // release: the header is visible
-#pragma unroll
-                        for (int m = 0; m < NMAT; ++m) {
-#pragma unroll
-                            for (int bx = 0; bx < P::NBOX; ++bx)
-                                tma_load_2d(st + m * P::WMAT + bx * 32 * kBoxB, tw[m], sl * (P::KC / 2) + bx * kBoxB,
-                                            tk.wrow, full + s);
-                            if (ws) tma_load_2d(st + P::OFF_WS + m * 32 * P::GRP * 2, ts[m], sl * P::GRP, tk.wrow, full + s);
-                        }
                     }
-                    if (lane < nb) {
-                        bulk_load(st + P::OFF_A + lane * P::KC * 2,
-                                  aq + static_cast<size_t>(arow) * act_row(tk.K) + sl * P::KC, ab, full + s);
-                        bulk_load(st + P::OFF_AM + lane * P::GRP * 8, am + static_cast<size_t>(arow) * ag_ld + sl * P::GRP,
+                    __syncwarp();
+                    // every copy of the stage from its own lane: one thread's copies are served one
+                    // after another, copies from different threads overlap
+                    const int brow = __shfl_sync(0xffffffffu, arow, lane & 3);
+                    if (lane < NMAT * P::NBOX) {
+                        const int m = lane / P::NBOX, bx = lane % P::NBOX;
+                        tma_load_2d(st + m * P::WMAT + bx * 32 * kBoxB, tw[m], sl * (P::KC / 2) + bx * kBoxB, tk.wrow,
+                                    full + s);
+                    } else if (lane >= kLaneScale && lane < kLaneScale + NMAT) {
+                        const int m = lane - kLaneScale;
+                        if (ws) tma_load_2d(st + P::OFF_WS + m * 32 * P::GRP * 2, ts[m], sl * P::GRP, tk.wrow, full + s);
+                    } else if (lane >= kLaneAct && lane < kLaneAct + nb) {
+                        const int b = lane - kLaneAct;
+                        bulk_load(st + P::OFF_A + b * P::KC * 2,
+                                  aq + static_cast<size_t>(brow) * act_row(tk.K) + sl * P::KC, ab, full + s);
+                    } else if (lane >= kLaneMeta && lane < kLaneMeta + nb) {
+                        const int b = lane - kLaneMeta;
+                        bulk_load(st + P::OFF_AM + b * P::GRP * 8, am + static_cast<size_t>(brow) * ag_ld + sl * P::GRP,
                                   mb, full + s);
                     }
                 }
             }
           }
+          q0 = __shfl_sync(0xffffffffu, qn, 0);
+        }
+        if (MODE != 1 && lane == 0) {
+            // the last CTA to stop claiming puts the counter back to zero for the next call
+            __threadfence();
+            if (atomicAdd(done_ctr, 1) == static_cast<int>(gridDim.x) - 1) {
+                atomicExch(next_ctr, 0);
+                atomicExch(done_ctr, 0);
+            }
         }
         // closing stage: a header with end = 1 and no copies
         if (!*abort_flag) {

@@ -111,6 +111,7 @@ struct GemvArgs {
     float* slot_term;             // COMBINE mode: [T*k][H] weighted, slot order
     float* sh_term;               // COMBINE mode: [T][H] gated shared rows
     int* col_counter;             // COMBINE mode: [H/32] zero between calls
+    int* task_counter;            // [4] task claim counters (gate/up, down), zero between calls
     int* status;                  // device status word (bounded-wait timeouts)
     const uint16_t* residual;     // COMBINE mode
     float* y;                     // COMBINE mode: [T][H]
