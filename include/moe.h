@@ -167,7 +167,8 @@ MOE_API int moe_dispatch_static(const int32_t* topk_ids, int T, int k, int E, in
 /* Expert MLP (stage 3) for every dispatched row, unweighted:
  *   rows fp32 [T*k][H]: rows[r] = W_d[e] (silu(W_g[e] x_t) * (W_u[e] x_t)) with
  *   a = perm[r], t = a / k, e the bucket holding r (offsets[e] <= r < offsets[e+1]).
- *   x bf16 [T][H]; offsets/perm as produced by moe_dispatch.
+ *   x bf16 [T][H], rows: 16-byte aligned (else MOE_ERR_INVALID_ARG);
+ *   offsets/perm as produced by moe_dispatch.
  *   arm: MOE_ARM_* (which kernels compute it). */
 MOE_API size_t moe_expert_mlp_workspace_size(int T, int k, int E, int H, int I);
 MOE_API int moe_expert_mlp(const uint16_t* x, int T, int k, const moe_experts* W,

@@ -334,7 +334,7 @@ int moe_expert_mlp(const uint16_t* x, int T, int k, const moe_experts* W, const 
     if (int s = check_experts(W)) return s;
     if (T < 0 || k < 1 || k > MOE_MAX_K || k > W->E) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    if (!x || !offsets || !perm || !rows || !ws || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+    if (!x || !offsets || !perm || !rows || !ws || !aligned16(x) || !aligned16(rows)) return MOE_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_expert_mlp_workspace_size(T, k, W->E, W->H, W->I)) return MOE_ERR_INVALID_ARG;
     const int a = choose_arm(arm, T, W->H, W->I, 0);

@@ -309,49 +309,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
         named_barrier(2, kDqThreads);  // row_slot / row_w visible to every epilogue thread
         // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp)
+        // The tile is staged in the pipeline's shared memory (free once the accumulators are
+        // final): row c = token row of the tile, 128 output columns; then each thread writes
+        // one token row with a bulk copy.  Gate/up stage fp16 h in the down GEMM's K order,
+        // down stages fp32 (weighted) outputs bound for the row's slot or token.
         bool go = __all_sync(0xffffffffu, ok);
         if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5));
+        go = named_barrier_or(2, kDqThreads, !go) ? false : go;  // all epilogue warps agree
         if (go) {
             tc_fence_after();
             const int q = warp & 3;                 // tensor-memory lane quadrant of this warp
             const int m = q * 32 + lane;            // accumulator row = weight row in the block
-            const int n_out = mblk * BM + m;        // output feature
             const int ch = (warp - 2) >> 2;         // column half handled by this warp
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
             const int cbeg = ch * (BN / 2), cend = min(nrows, cbeg + BN / 2);
-            for (int c0 = cbeg; c0 < cend; c0 += 16) {
-                float d0[16];
-                tmem_ld16(tbase + c0, d0);
-                if (MODE == 0) {
-                    float d1[16];
-                    tmem_ld16(tbase + BN + c0, d1);
-                    uint16_t* hout = shared ? p.h_s : p.h_r;
-                    const int pos = (n_out & ~7) + kperm8(n_out & 7);  // K order of the down GEMM
-                    if (n_out < M) {
+            if (MODE == 0) {
+                uint16_t* stile = reinterpret_cast<uint16_t*>(smem);           // [BN][BM] fp16
+                const int pos = (m & ~7) + kperm8(m & 7);                     // K order of the down GEMM
+                for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                    float g[32], u[32];
+                    tmem_ld32x2(tbase + c0, tbase + BN + c0, g, u);
 #pragma unroll
-                        for (int cc = 0; cc < 16; ++cc) {
-                            const int c = c0 + cc;
-                            if (c < cend) {
-                                const float g = d0[cc], u = d1[cc];
-                                const float h = g / (1.f + expf(-g)) * u;
-                                hout[static_cast<size_t>(row0 + c) * M + pos] = __half_as_ushort(__float2half_rn(h));
-                            }
-                        }
-                    }
-                } else if (n_out < M) {
-#pragma unroll
-                    for (int cc = 0; cc < 16; ++cc) {
-                        const int c = c0 + cc;
-                        if (c >= cend) continue;
-                        if (shared) {
-                            p.out_s[static_cast<size_t>(row0 + c) * M + n_out] = row_w[c] * d0[cc];
-                        } else if (p.out_mode == 0) {
-                            p.out_r[static_cast<size_t>(row0 + c) * M + n_out] = d0[cc];
-                        } else {
-                            p.out_r[static_cast<size_t>(row_slot[c]) * M + n_out] = row_w[c] * d0[cc];
+                    for (int cc = 0; cc < 32; ++cc) {
+                        if (c0 + cc < cend) {
+                            const float h = __fdividef(g[cc] * u[cc], 1.f + __expf(-g[cc]));
+                            stile[(c0 + cc) * BM + pos] = __half_as_ushort(__float2half_rn(h));
                         }
                     }
                 }
+            } else {
+                float* stile = reinterpret_cast<float*>(smem);                 // [BN][BM] fp32
+                const bool weighted = shared || p.out_mode == 1;
+                for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                    float d[32];
+                    tmem_ld32(tbase + c0, d);
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc) {
+                        if (c0 + cc < cend) stile[(c0 + cc) * BM + m] = weighted ? row_w[c0 + cc] * d[cc] : d[cc];
+                    }
+                }
+            }
+            fence_proxy_async_smem();  // the tile's generic writes, before the bulk copies read it
+            named_barrier(2, kDqThreads);
+            if (dt < nrows) {
+                const int cols = min(BM, M - mblk * BM);
+                if (MODE == 0) {
+                    uint16_t* hout = shared ? p.h_s : p.h_r;
+                    bulk_store(hout + static_cast<size_t>(row0 + dt) * M + mblk * BM,
+                               reinterpret_cast<const uint16_t*>(smem) + dt * BM, cols * 2);
+                } else {
+                    const size_t orow = shared ? static_cast<size_t>(row0 + dt)
+                                               : (p.out_mode == 1 ? static_cast<size_t>(row_slot[dt])
+                                                                  : static_cast<size_t>(row0 + dt));
+                    float* out = shared ? p.out_s : p.out_r;
+                    bulk_store(out + orow * M + mblk * BM, reinterpret_cast<const float*>(smem) + dt * BM, cols * 4);
+                }
+                bulk_store_wait();
             }
         }
     }
