@@ -41,6 +41,7 @@ constexpr int kTileBytesB = BN * BK * 2;
 constexpr int kStagesGU = 3;
 constexpr int kStagesDN = 4;
 constexpr int kDqThreads = 256;                 // dequantising / epilogue threads (warps 2..9)
+constexpr int kPrefetch = 4;                    // K-steps of raw weights in flight per thread
 constexpr int kGemmThreads = 64 + kDqThreads;   // + TMA warp + MMA warp
 
 struct GemmK {
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_a + s, kDqThreads);
+            mbar_init(full_a + s, kDqThreads / 32);  // one arrival per dequantising warp
             mbar_init(full_b + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -286,26 +287,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                 }
             }
         }
-        RawK ra = load_raw(qa, sa, 0, half, valid), rb{};
-        if (MODE == 0) rb = load_raw(qb, sb, 0, half, valid);
+        // raw weights kPrefetch K-steps ahead in registers; one lane per warp waits for a free
+        // stage and one arrives for the warp (after __syncwarp orders the warp's writes), so
+        // that 256 threads do not poll and arrive on one barrier word every K-step
+        RawK ra[kPrefetch], rb[kPrefetch];
+#pragma unroll
+        for (int d = 0; d < kPrefetch; ++d) {
+            ra[d] = load_raw(qa, sa, d, half, valid && d < nk);
+            if (MODE == 0) rb[d] = load_raw(qb, sb, d, half, valid && d < nk);
+        }
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % S;
-            RawK na{}, nb{};
-            if (kb + 1 < nk) {
-                na = load_raw(qa, sa, kb + 1, half, valid);
-                if (MODE == 0) nb = load_raw(qb, sb, kb + 1, half, valid);
+        for (int kb0 = 0; kb0 < nk && ok; kb0 += kPrefetch) {
+#pragma unroll
+            for (int d = 0; d < kPrefetch; ++d) {
+                const int kb = kb0 + d;
+                if (kb >= nk) break;
+                const int s = kb % S;
+                if (kb >= S) {
+                    bool free_ok = true;
+                    if (lane == 0) free_ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4);
+                    if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                store_dequant(stage_a(s, 0), pr, half, ra[d]);
+                if (MODE == 0) store_dequant(stage_a(s, 1), pr, half, rb[d]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_a + s);
+                if (kb + kPrefetch < nk) {
+                    ra[d] = load_raw(qa, sa, kb + kPrefetch, half, valid);
+                    if (MODE == 0) rb[d] = load_raw(qb, sb, kb + kPrefetch, half, valid);
+                }
             }
-            if (kb >= S && !mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4)) {
-                ok = false;
-                break;
-            }
-            store_dequant(stage_a(s, 0), pr, half, ra);
-            if (MODE == 0) store_dequant(stage_a(s, 1), pr, half, rb);
-            fence_proxy_async_smem();
-            mbar_arrive(full_a + s);
-            ra = na;
-            if (MODE == 0) rb = nb;
         }
         named_barrier(2, kDqThreads);  // row_slot / row_w visible to every epilogue thread
         // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp)
