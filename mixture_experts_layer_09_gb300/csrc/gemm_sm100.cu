@@ -18,9 +18,10 @@
 // top-k weight in slot order (the tensor arm's combine feed), or the shared expert's rows
 // scaled by sigmoid of its gate logit.
 //
-// Roles in a CTA of 320 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
-// memory and issues the MMAs (one thread), warps 2-9 dequantise A (two threads per weight
-// row) and then run the epilogue (each warp one TMEM lane quadrant and half the columns).
+// Roles in a CTA of 576 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
+// memory and issues the MMAs (one thread), warps 2-17 dequantise A (four threads per weight
+// row: with one CTA per SM the dequantisation is latency-bound, so more warps carry it) and
+// then run the epilogue (each warp one TMEM lane quadrant and a quarter of the columns).
 // Every mbarrier wait is bounded; a wait that runs out records MOE_ERR_DEVICE_TIMEOUT in the
 // status word, stops the CTA's loops, drains its own copies and MMAs, frees its tensor
 // memory and returns.
@@ -40,7 +41,12 @@ constexpr int kTileBytesA = BM * BK * 2;
 constexpr int kTileBytesB = BN * BK * 2;
 constexpr int kStagesGU = 3;
 constexpr int kStagesDN = 4;
-constexpr int kDqThreads = 256;                 // dequantising / epilogue threads (warps 2..9)
+#ifndef MOE_GEMM_TPR
+#define MOE_GEMM_TPR 4
+#endif
+constexpr int kTpr = MOE_GEMM_TPR;              // dequantising threads per weight row
+constexpr int kCpt = 8 / kTpr;                  // 16-byte chunks (8 K-columns) per thread per K-step
+constexpr int kDqThreads = BM * kTpr;           // dequantising / epilogue threads (warps 2..)
 constexpr int kPrefetch = 4;                    // K-steps of raw weights in flight per thread
 constexpr int kGemmThreads = 64 + kDqThreads;   // + TMA warp + MMA warp
 
@@ -102,33 +108,41 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
 // Position of column c (0..7) of an 8-column group in that K order.
 __host__ __device__ constexpr inline int kperm8(int c) { return (c & 3) * 2 + (c >> 2); }
 
-// One K-step (64 columns) of half a weight row: 16 bytes of nibbles and the group's scale.
+// One K-step (64 columns) of a thread's part of a weight row: kCpt words of nibbles (8 columns
+// each) and the scale of their group (a part never straddles two 32-column groups).
 struct RawK {
-    uint4 q;
+    uint32_t q[kCpt];
     uint16_t s;
 };
 
-__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, int half, bool valid) {
+__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, int part, bool valid) {
     RawK r;
     if (valid) {
-        r.q = ldg_nc(qrow + kb * 32 + half * 16);
-        r.s = __ldg(srow + kb * 2 + half);
+        const uint8_t* src = qrow + kb * 32 + part * kCpt * 4;
+        if constexpr (kCpt == 4) {
+            const uint4 v = ldg_nc(src);
+            r.q[0] = v.x; r.q[1] = v.y; r.q[2] = v.z; r.q[3] = v.w;
+        } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+            r.q[0] = v.x; r.q[1] = v.y;
+        }
+        r.s = __ldg(srow + kb * 2 + (part * kCpt) / 4);
     } else {
-        r.q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);  // all zero weights
+#pragma unroll
+        for (int j = 0; j < kCpt; ++j) r.q[j] = 0x88888888u;  // all zero weights
         r.s = 0;
     }
     return r;
 }
 
-// Writes chunks half*4 .. half*4+3 of `row` into a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int half, const RawK& r) {
+// Writes chunks part*kCpt .. part*kCpt+kCpt-1 of `row` into a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int part, const RawK& r) {
     const __half2 s2 = __half2half2(__ushort_as_half(r.s));
-    const uint32_t w[4] = {r.q.x, r.q.y, r.q.z, r.q.w};
     uint8_t* rowp = tile + row * 128;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int c = half * 4 + j;
-        *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = dequant8(w[j], s2);
+    for (int j = 0; j < kCpt; ++j) {
+        const int c = part * kCpt + j;
+        *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = dequant8(r.q[j], s2);
     }
 }
 
@@ -259,7 +273,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     } else {
         // ---------------- A producers (8 warps: two threads per weight row), then the epilogue
         const int dt = threadIdx.x - 64;
-        const int pr = dt >> 1, half = dt & 1;  // weight row within the block, half of its K-step
+        const int pr = dt / kTpr, half = dt % kTpr;  // weight row within the block, part of its K-step
         const int wrow = mblk * BM + pr;        // weight row within the matrix
         const bool valid = wrow < M;
         const size_t grow = shared ? static_cast<size_t>(wrow) : static_cast<size_t>(e) * M + wrow;
@@ -335,9 +349,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             tc_fence_after();
             const int q = warp & 3;                 // tensor-memory lane quadrant of this warp
             const int m = q * 32 + lane;            // accumulator row = weight row in the block
-            const int ch = (warp - 2) >> 2;         // column half handled by this warp
+            const int ch = (warp - 2) >> 2;         // column share handled by this warp
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            const int cbeg = ch * (BN / 2), cend = min(nrows, cbeg + BN / 2);
+            constexpr int kCols = BN / (kDqThreads / 128);
+            const int cbeg = ch * kCols, cend = min(nrows, cbeg + kCols);
             if (MODE == 0) {
                 uint16_t* stile = reinterpret_cast<uint16_t*>(smem);           // [BN][BM] fp16
                 const int pos = (m & ~7) + kperm8(m & 7);                     // K order of the down GEMM
