@@ -109,28 +109,32 @@ __global__ void __launch_bounds__(1024) topk_dispatch_kernel(const float* __rest
                                                              int32_t* active, int32_t* n_active, int* status) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ int hist[];  // [32][E]
+    // the ids stay in shared memory between the top-k and the two walks; warp r walks slots
+    // 32r .. 32r+31, so only ceil(T*k / 32) histogram rows are in use
+    extern __shared__ int hist[];  // [rows][E]
+    __shared__ int ids_s[1024];
     __shared__ int scratch[9];
     const int wid = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) hist[i] = 0;
-    if (wid < T)
-        topk_warp_row<float, VPT>(logits + static_cast<size_t>(wid) * ld, E, k, ids + static_cast<size_t>(wid) * k,
-                                  w + static_cast<size_t>(wid) * k);
-    __syncthreads();  // the ids written above are visible to the whole CTA from here
     const int n = T * k;
-    const int per = ((n + 31) / 32 + 31) / 32 * 32;
-    const int begin = min(n, wid * per), end = min(n, begin + per);
-    warp_walk(ids, begin, end, E, hist + wid * E, 0, perm, inv, status);
+    const int rows = (n + 31) / 32;
+    for (int i = threadIdx.x; i < rows * E; i += blockDim.x) hist[i] = 0;
+    if (wid < T)
+        topk_warp_row<float, VPT>(logits + static_cast<size_t>(wid) * ld, E, k, ids_s + wid * k,
+                                  w + static_cast<size_t>(wid) * k);
     __syncthreads();
-    finalize_plan(hist, 32, E, n, counts, offsets, active, n_active, scratch);
+    if (static_cast<int>(threadIdx.x) < n) ids[threadIdx.x] = ids_s[threadIdx.x];
+    const int begin = min(n, wid * 32), end = min(n, begin + 32);
+    warp_walk(ids_s, begin, end, E, hist + wid * E, 0, perm, inv, status, true);
     __syncthreads();
-    warp_walk(ids, begin, end, E, hist + wid * E, 1, perm, inv, status);
+    finalize_plan(hist, rows, E, n, counts, offsets, active, n_active, scratch);
+    __syncthreads();
+    warp_walk(ids_s, begin, end, E, hist + wid * E, 1, perm, inv, status, true);
 }
 
 cudaError_t launch_topk_dispatch(const float* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
                                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
                                  int32_t* n_active, int* status, cudaStream_t st) {
-    const size_t smem = 32 * E * sizeof(int);
+    const size_t smem = static_cast<size_t>((T * k + 31) / 32) * E * sizeof(int);
     const int vpt = (E + 31) / 32;
     KernelScope ks_("topk_dispatch", st);
     switch (vpt) {

@@ -111,16 +111,18 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
 // ------------------------------------------------------------------ dispatch pieces
 // Walk a warp's slot run 32 at a time.  mode 0: count into hist; mode 1: scatter using hist
 // as the running base (hist must hold the warp's starting position per expert).
+// (ids_in_smem: the ids sit in this CTA's shared memory; otherwise they are read from global
+// memory with coherent loads, since they may have been written by the same kernel)
 __device__ __forceinline__ void warp_walk(const int32_t* ids, int begin, int end, int E,
                                           int* hist, int mode, int32_t* __restrict__ perm,
-                                          int32_t* __restrict__ inv, int* status) {
+                                          int32_t* __restrict__ inv, int* status, bool ids_in_smem = false) {
     const int lane = threadIdx.x & 31;
     const unsigned lt = lanemask_lt();
     for (int base = begin; base < end; base += 32) {
         const int a = base + lane;
         int id = -1;
         if (a < end) {
-            id = __ldcg(ids + a);  // coherent: the ids may come from the same kernel
+            id = ids_in_smem ? ids[a] : __ldcg(ids + a);
             if (id < 0 || id >= E) {
                 if (mode == 0) record_status(status, MOE_ERR_DEVICE_INDEX, a, id);
                 id = -1;

@@ -20,19 +20,22 @@
 namespace moe {
 
 // ------------------------------------------------------------------ logits, decode GEMV
-// One CTA (128 threads) per router row; thread c covers 16-byte chunks c, c+128, ... of H.
-// CTAs past the router rows quantise x for the GEMV arm (4 warps, one (token, group of 32)
-// each) when xq != nullptr, so that step costs no launch of its own.
+// Decode batches: one CTA per router row (and one for the gate row) reads the row once and
+// dots it with every token in one pass (TB >= T); 256 threads, one 16-byte chunk of the row
+// per thread per 2048 columns; the eight warp sums meet in a fixed order.  CTAs past the rows
+// quantise x for the GEMV arm (one 32-value group per warp) when xq != nullptr, so that step
+// costs no launch of its own.
 template <int TB>
-__global__ void __launch_bounds__(128) router_logits_gemv_kernel(
+__global__ void __launch_bounds__(256) router_logits_gemv_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
     int T, int H, int E, int ld, float* __restrict__ logits, int nrows, int16_t* __restrict__ xq,
     int2* __restrict__ xmeta, int x_gld) {
     pdl_wait();
     pdl_trigger();
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (static_cast<int>(blockIdx.x) >= nrows) {
-        const int ng = H / 32, lane = threadIdx.x & 31;
-        const int gw = (blockIdx.x - nrows) * 4 + (threadIdx.x >> 5);
+        const int ng = H / 32;
+        const int gw = (blockIdx.x - nrows) * 8 + wid;
         if (gw >= T * ng) return;
         const int t = gw / ng, grp = gw % ng;
         const float v = bf16_to_f32(x[static_cast<size_t>(t) * H + grp * 32 + lane]);
@@ -43,45 +46,42 @@ __global__ void __launch_bounds__(128) router_logits_gemv_kernel(
     const int row = blockIdx.x;  // 0..E-1 router rows, E = gate row
     const uint16_t* w = (row < E) ? W_r + static_cast<size_t>(row) * H : g;
     const int nch = H / 8;
-    __shared__ float red[4][TB];
-    for (int t0 = 0; t0 < T; t0 += TB) {
-        float acc[TB];
+    __shared__ float red[8][TB];
+    float acc[TB];
 #pragma unroll
-        for (int i = 0; i < TB; ++i) acc[i] = 0.f;
-        for (int c = threadIdx.x; c < nch; c += 128) {
-            uint4 wv = ldg_nc(w + static_cast<size_t>(c) * 8);
-            float wf[8];
-            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    for (int i = 0; i < TB; ++i) acc[i] = 0.f;
+    for (int c = threadIdx.x; c < nch; c += 256) {
+        const uint4 wv = ldg_nc(w + static_cast<size_t>(c) * 8);
+        float wf[8];
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                wf[2 * q] = __uint_as_float(ww[q] << 16);
-                wf[2 * q + 1] = __uint_as_float(ww[q] & 0xffff0000u);
-            }
+        for (int q = 0; q < 4; ++q) {
+            wf[2 * q] = __uint_as_float(ww[q] << 16);
+            wf[2 * q + 1] = __uint_as_float(ww[q] & 0xffff0000u);
+        }
 #pragma unroll
-            for (int i = 0; i < TB; ++i) {
-                if (t0 + i < T) {
-                    uint4 xv = ldg_nc(x + static_cast<size_t>(t0 + i) * H + static_cast<size_t>(c) * 8);
-                    const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+        for (int i = 0; i < TB; ++i) {
+            if (i < T) {
+                const uint4 xv = ldg_nc(x + static_cast<size_t>(i) * H + static_cast<size_t>(c) * 8);
+                const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[i] = fmaf(__uint_as_float(xx[q] << 16), wf[2 * q], acc[i]);
-                        acc[i] = fmaf(__uint_as_float(xx[q] & 0xffff0000u), wf[2 * q + 1], acc[i]);
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    acc[i] = fmaf(__uint_as_float(xx[q] << 16), wf[2 * q], acc[i]);
+                    acc[i] = fmaf(__uint_as_float(xx[q] & 0xffff0000u), wf[2 * q + 1], acc[i]);
                 }
             }
         }
-        const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    }
 #pragma unroll
-        for (int i = 0; i < TB; ++i) {
-            float v = warp_sum(acc[i]);
-            if (lane == 0) red[wid][i] = v;
-        }
-        __syncthreads();
-        if (threadIdx.x < TB && t0 + threadIdx.x < T) {
-            const int i = threadIdx.x;
-            logits[static_cast<size_t>(t0 + i) * ld + row] = (red[0][i] + red[1][i]) + (red[2][i] + red[3][i]);
-        }
-        __syncthreads();
+    for (int i = 0; i < TB; ++i) {
+        const float v = warp_sum(acc[i]);
+        if (lane == 0) red[wid][i] = v;
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < T) {
+        const int i = threadIdx.x;
+        logits[static_cast<size_t>(i) * ld + row] =
+            ((red[0][i] + red[1][i]) + (red[2][i] + red[3][i])) + ((red[4][i] + red[5][i]) + (red[6][i] + red[7][i]));
     }
 }
 
@@ -162,13 +162,20 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const u
     const int nrows = E + (g ? 1 : 0);
     const int ld = nrows;
     if (T <= 32) {
-        const int qctas = xq ? (T * (H / 32) + 3) / 4 : 0;
+        const int qctas = xq ? (T * (H / 32) + 7) / 8 : 0;
         KernelScope ks_(xq ? "router_logits_gemv+quant_x" : "router_logits_gemv", st);
+        const dim3 grid(nrows + qctas), block(256);
         if (T <= 4)
-            return launch_pdl(router_logits_gemv_kernel<4>, dim3(nrows + qctas), dim3(128), 0, st, x, W_r, g, T, H, E,
-                              ld, logits, nrows, xq, xmeta, x_gld);
-        return launch_pdl(router_logits_gemv_kernel<8>, dim3(nrows + qctas), dim3(128), 0, st, x, W_r, g, T, H, E, ld,
-                          logits, nrows, xq, xmeta, x_gld);
+            return launch_pdl(router_logits_gemv_kernel<4>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
+                              xq, xmeta, x_gld);
+        if (T <= 8)
+            return launch_pdl(router_logits_gemv_kernel<8>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
+                              xq, xmeta, x_gld);
+        if (T <= 16)
+            return launch_pdl(router_logits_gemv_kernel<16>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
+                              xq, xmeta, x_gld);
+        return launch_pdl(router_logits_gemv_kernel<32>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows, xq,
+                          xmeta, x_gld);
     }
     cudaError_t e;
     if (router_tc_supported(x, W_r, g, H, E)) {
