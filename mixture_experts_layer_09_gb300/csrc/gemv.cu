@@ -244,14 +244,18 @@ __device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt
     named_barrier(1, kCW * 32);
 }
 
-// One full slice with staged scales for NB tokens: every chunk of the lane, no branches.
+// One slice with staged scales for NB tokens: chunks ks, ks + 8, ... below nch (a slice
+// shorter than KC, as the last or only slice of a short K, ends early; when nch is a multiple
+// of 8 every lane stops at the same chunk).
 template <int MODE, int NB>
-__device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, float (&acc)[Pipe<MODE>::TB][Pipe<MODE>::NMAT]) {
+__device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, int nch,
+                                          float (&acc)[Pipe<MODE>::TB][Pipe<MODE>::NMAT]) {
     using P = Pipe<MODE>;
     constexpr int NMAT = P::NMAT;
 #pragma unroll
     for (int j = 0; j < P::CPL; ++j) {
         const int c = ks + 8 * j;
+        if (c >= nch) break;
         Nib nw[NMAT];
         float fs[NMAT];
 #pragma unroll
@@ -570,13 +574,13 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         }
         const bool ws = hd->shared ? ((MODE == 0) ? p.ws_sh_gu : p.ws_sh_d) : ((MODE == 0) ? p.ws_gu : p.ws_d);
         const int nch = min(P::KC, K - sl * P::KC) / 32;
-        if (ws && nch == P::KC / 32) {
-            // full slice with staged scales: branch-free, specialised on the token count
+        if (ws) {
+            // staged scales: specialised on the token count
             switch (nb) {
-                case 1: stage_dot<MODE, 1>(st, ks, lrow, acc); break;
-                case 2: stage_dot<MODE, 2>(st, ks, lrow, acc); break;
-                case 3: stage_dot<MODE, 3>(st, ks, lrow, acc); break;
-                default: stage_dot<MODE, 4>(st, ks, lrow, acc); break;
+                case 1: stage_dot<MODE, 1>(st, ks, lrow, nch, acc); break;
+                case 2: stage_dot<MODE, 2>(st, ks, lrow, nch, acc); break;
+                case 3: stage_dot<MODE, 3>(st, ks, lrow, nch, acc); break;
+                default: stage_dot<MODE, 4>(st, ks, lrow, nch, acc); break;
             }
         } else {
 #pragma unroll
