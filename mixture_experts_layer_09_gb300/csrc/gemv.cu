@@ -173,7 +173,7 @@ struct Pipe {
     static constexpr int STAGE = (OFF_HDR + 256 + 1023) / 1024 * 1024;
     static constexpr int STAGES = (MODE == 0) ? 4 : 3;  // two CTAs fit one SM
     static_assert(OFF_WS % 128 == 0 && OFF_A % 128 == 0 && OFF_AM % 16 == 0, "copy destinations aligned");
-    static_assert(NMAT * NBOX <= kLaneScale && TB <= 8, "one copy per producer lane");
+    static_assert(NMAT * NBOX <= kLaneScale && TB == 4, "one copy per producer lane; four tokens per pass");
 };
 
 struct StageHdr {
@@ -191,7 +191,28 @@ struct StageHdr {
 struct TaskDesc {
     bool shared;
     int e, rb, K, b0, b1, wrow;
+    int arow0[4], slot0[4];  // the first pass's tokens: activation rows and (down) slots
+    float wgt0[4];           // and (down) their weights or the shared gate
 };
+
+// Activation row, slot and weight of bucket row r of a task (r < b1).
+template <int MODE>
+__device__ __forceinline__ void pass_row(const GemvArgs& p, bool shared, int r, int& arow, int& slot, float& wgt) {
+    slot = 0;
+    wgt = 0.f;
+    if (MODE == 0) {
+        arow = shared ? r : __ldg(p.perm + r) / p.k;
+    } else {
+        arow = r;
+        if (shared) {
+            wgt = 1.f;
+            if (p.sh_gate_logit) wgt = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
+        } else if (MODE == 1) {
+            slot = __ldg(p.perm + r);
+            wgt = __ldg(p.topk_w + slot);
+        }
+    }
+}
 
 template <int MODE>
 __device__ __forceinline__ void task_desc(const GemvArgs& p, int t, int n_act, int nrb, TaskDesc& tk) {
@@ -213,6 +234,14 @@ __device__ __forceinline__ void task_desc(const GemvArgs& p, int t, int n_act, i
         tk.b1 = p.T;
         tk.K = (MODE == 0) ? p.H : p.sh_I;
         tk.wrow = tk.rb * 32;
+    }
+    // the first pass's per-token loads now, with the descriptor, not on the producer's path
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        tk.arow0[i] = 0;
+        tk.slot0[i] = 0;
+        tk.wgt0[i] = 0.f;
+        if (tk.b0 + i < tk.b1) pass_row<MODE>(p, tk.shared, tk.b0 + i, tk.arow0[i], tk.slot0[i], tk.wgt0[i]);
     }
 }
 
@@ -279,16 +308,17 @@ __device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, i
     }
 }
 
-// MODE 1: this CTA's contiguous range [first, last) of the column-block-major task list, cut at
-// equal shares of the estimated work.  A task costs about (4 + tokens) per pass of up to four
-// tokens and per K-slice; every column block holds one task of each active expert (and of the
-// shared expert), so all blocks cost the same and a cut point maps to (block, expert) by one
-// count over the experts' cost prefix.  Runs on the producer warp; n_act <= 256.
-__device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int nrb, int per_cb, int lane, int& first,
+// Down projection with the folded combine: this CTA's contiguous range [first, last) of the
+// column-block-major task list (block cb: one task of each active expert, then the shared
+// one), cut at equal shares of the estimated work.  A task costs about (4 + tokens) per pass
+// of up to four tokens and per K-slice, so every block costs the same and a cut point maps to
+// (block, expert) by one count over the experts' cost prefix.  Runs on the producer warp;
+// n_act <= 256 (eight experts per lane).
+__device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int nrb, int nsh, int lane, int& first,
                                                int& last) {
-    constexpr int KC = kSliceH;
-    const int nsl_r = (p.I + KC - 1) / KC;
-    long long pre[8];  // exclusive cost prefix of experts lane*8 .. lane*8+7
+    constexpr int KC = Pipe<1>::KC;
+    const long long nsl_r = (p.I + KC - 1) / KC;
+    long long pre[8];  // exclusive cost prefix within the lane
     long long mine = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -297,7 +327,7 @@ __device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int
         if (a < n_act) {
             const int e = __ldg(p.active + a);
             const int cnt = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
-            mine += static_cast<long long>(nsl_r) * (4 * ((cnt + 3) / 4) + cnt);
+            mine += nsl_r * (4 * ((cnt + 3) / 4) + cnt);
         }
     }
     long long incl = mine;
@@ -309,9 +339,10 @@ __device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int
     const long long base = incl - mine;
     const long long routed = __shfl_sync(0xffffffffu, incl, 31);
     long long W = routed;
-    if (p.sh_I > 0) W += static_cast<long long>((p.sh_I + KC - 1) / KC) * (4 * ((p.T + 3) / 4) + p.T);
+    if (nsh > 0) W += static_cast<long long>((p.sh_I + KC - 1) / KC) * (4 * ((p.T + 3) / 4) + p.T);
     if (W <= 0) W = 1;
     const long long C = W * nrb;
+    const int per_cb = n_act + (nsh > 0 ? 1 : 0);
     auto cut = [&](long long pos) -> int {  // first task whose start cost is >= pos
         if (pos >= C) return nrb * per_cb;
         const long long cb = pos / W, rem = pos - cb * W;
@@ -320,7 +351,7 @@ __device__ __forceinline__ void balanced_range(const GemvArgs& p, int n_act, int
         for (int i = 0; i < 8; ++i) n += (lane * 8 + i < n_act && base + pre[i] < rem) ? 1 : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-        if (per_cb > n_act && routed < rem) ++n;  // the shared expert's task
+        if (nsh > 0 && routed < rem) ++n;  // the shared expert's task
         return static_cast<int>(cb) * per_cb + n;
     };
     first = cut(C * blockIdx.x / gridDim.x);
@@ -359,19 +390,18 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         const int nsh = (p.sh_I > 0) ? ((MODE == 0) ? p.sh_I / 32 : p.H / 32) : 0;
         const int ntask = n_act * nrb + nsh;
         const int per_cb = n_act + (nsh > 0 ? 1 : 0);
-        // tasks are claimed in chunks from a counter in the workspace head, the next chunk
-        // claimed while the current one streams: tasks differ in token count, so a fixed split
-        // of the list leaves some CTAs with twice the work of others
+        // Gate/up (and the rows-mode down) claim chunks of tasks from a counter in the workspace
+        // head, the next chunk claimed while the current one streams, the first chunk implied by
+        // the CTA index: tasks differ in token count, and a fixed split left the slowest CTA far
+        // behind the mean.  The down projection with the folded combine instead walks one
+        // contiguous column-block-major range per CTA (it leaves each block at most once), cut by
+        // estimated cost above four tokens and by task count below.
         int* next_ctr = p.task_counter + (MODE == 0 ? 0 : 2);
         int* done_ctr = next_ctr + 1;
-        // (the down projection with the folded combine instead walks one contiguous range per
-        // CTA, so that it leaves each column block at most once; above four tokens a task's
-        // cost depends on its token count and the ranges are cut by cost)
-        int CH = max(1, min(32, ntask / (static_cast<int>(gridDim.x) * 8)));
-        int q0, r_last = ntask;
+        int CH, q0, r_last = ntask;
         if (MODE == 1) {
             if (p.T > 4) {
-                balanced_range(p, n_act, nrb, per_cb, lane, q0, r_last);
+                balanced_range(p, n_act, nrb, nsh, lane, q0, r_last);
             } else {
                 const int len = (ntask + gridDim.x - 1) / gridDim.x;
                 q0 = min(ntask, static_cast<int>(blockIdx.x) * len);
@@ -379,13 +409,15 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
             }
             CH = 32;
         } else {
-            q0 = static_cast<int>(blockIdx.x) * CH;  // first chunk: implied by the CTA index
+            CH = max(1, min(32, ntask / (static_cast<int>(gridDim.x) * 8)));
+            q0 = static_cast<int>(blockIdx.x) * CH;
         }
         uint32_t it = 0;
         while (q0 < r_last && !*abort_flag) {
-          int qn = 0;
-          if (MODE != 1 && lane == 0) qn = atomicAdd(next_ctr, CH) + static_cast<int>(gridDim.x) * CH;
-          if (MODE == 1) qn = q0 + CH;
+          int qn = q0 + CH;
+          if (MODE != 1) {
+              if (lane == 0) qn = atomicAdd(next_ctr, CH) + static_cast<int>(gridDim.x) * CH;
+          }
           const int last = min(r_last, q0 + CH);
           // the warp's lanes look up the chunk's task descriptors at once
           TaskDesc mine{};
@@ -429,26 +461,25 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                 ag_ld = tk.shared ? p.sh_gld : p.h_gld;
             }
             const int nsl = (tk.K + P::KC - 1) / P::KC;
+            // the first pass's token data from the descriptor lane: lane b takes token b
+            int farow = 0, fslot = 0;
+            float fwgt = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int va = __shfl_sync(0xffffffffu, mine.arow0[i], j);
+                const int vs = __shfl_sync(0xffffffffu, mine.slot0[i], j);
+                const float vw = __shfl_sync(0xffffffffu, mine.wgt0[i], j);
+                if (lane == i) {
+                    farow = va;
+                    fslot = vs;
+                    fwgt = vw;
+                }
+            }
             for (int t0 = tk.b0; t0 < tk.b1 && !*abort_flag; t0 += TB) {
                 const int nb = min(TB, tk.b1 - t0);
-                int arow = 0, slot = 0;
-                float wgt = 0.f;
-                if (lane < nb) {
-                    const int r = t0 + lane;
-                    if (MODE == 0) {
-                        arow = tk.shared ? r : __ldg(p.perm + r) / p.k;
-                    } else {
-                        arow = r;
-                        if (tk.shared) {
-                            wgt = 1.f;
-                            if (p.sh_gate_logit)
-                                wgt = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
-                        } else if (MODE == 1) {
-                            slot = __ldg(p.perm + r);
-                            wgt = __ldg(p.topk_w + slot);
-                        }
-                    }
-                }
+                int arow = farow, slot = fslot;
+                float wgt = fwgt;
+                if (t0 != tk.b0 && lane < nb) pass_row<MODE>(p, tk.shared, t0 + lane, arow, slot, wgt);
                 for (int sl = 0; sl < nsl; ++sl, ++it) {
                     const int s = it % S;
                     if (it >= static_cast<uint32_t>(S)) {
@@ -502,7 +533,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                 }
             }
           }
-          q0 = __shfl_sync(0xffffffffu, qn, 0);
+          q0 = (MODE == 1) ? qn : __shfl_sync(0xffffffffu, qn, 0);
         }
         if (MODE != 1 && lane == 0) {
             // the last CTA to stop claiming puts the counter back to zero for the next call
@@ -642,12 +673,14 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         // ---- end of a pass
         if (MODE == 0) {
 #pragma unroll
-            for (int b = 0; b < TB; ++b)
+            for (int b = 0; b < TB; ++b) {
+                if (b >= nb) break;  // the pass's token count (warp-uniform)
 #pragma unroll
                 for (int m = 0; m < NMAT; ++m) {
                     const float v = row_sum8(acc[b][m]);
                     if (ks == 0) red[(b * 2 + m) * 32 + lrow] = v;
                 }
+            }
             named_barrier(1, kCW * 32);
             if (warp < nb) {
                 const int b = warp;
@@ -664,8 +697,9 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
             const int n = rb * 32 + lrow;  // output column of this lane group
 #pragma unroll
             for (int b = 0; b < TB; ++b) {
+                if (b >= nb) break;  // the pass's token count (warp-uniform)
                 const float o = row_sum8(acc[b][0]);
-                if (ks == 0 && b < nb) {
+                if (ks == 0) {
                     const int r = t0 + b;
                     if (shared) {
                         float* dst = (MODE == 1) ? p.sh_term : p.sh_rows_out;
