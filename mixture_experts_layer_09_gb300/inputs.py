@@ -165,6 +165,18 @@ def set_bias_channel(x: np.ndarray, W_r: np.ndarray, bias: np.ndarray) -> None:
     W_r[:, 0] = bf16_bits(np.asarray(bias, dtype=np.float32))
 
 
+def zipf_bias(E: int, s: float, H: int) -> np.ndarray:
+    """Router bias for a Zipf(s)-like expert popularity: expert e gets -s * sigma * ln(e + 1),
+    sigma = 0.02 * sqrt(H) the spread of a router logit (router rows ~N(0, 0.02), x ~N(0, 1)),
+    expert 0 the most popular.  At H=256, E=8, k=2 the slot shares come out near Zipf(1.1)'s
+    (0.38 0.23 0.15 0.08 0.07 0.04 0.03 0.03 against 0.40 0.19 0.12 0.09 0.07 0.06 0.05 0.04)."""
+    sigma = 0.02 * np.sqrt(H)
+    return (-s * sigma * np.log(np.arange(E, dtype=np.float64) + 1.0)).astype(np.float32)
+
+
+ONE_BF16 = 0x3F80  # bf16 bits of 1.0, the bias channel's hidden value
+
+
 # ----------------------------------------------------------------------------- workloads
 
 @dataclass
@@ -176,6 +188,7 @@ class Workload:
     E: int
     k: int
     I_sh: int = 0
+    zipf: float = 0.0  # > 0: skewed popularity through the bias channel (set_bias_channel)
     gated_shared: bool = True
     residual: bool = True
     seed: int = 0
@@ -199,7 +212,7 @@ WORKLOADS = {
     "qwen15_prefill_t512": Workload("qwen15_prefill_t512", 512, 2048, 1408, 60, 4, I_sh=5632),
     "qwen15_prefill_t4096": Workload("qwen15_prefill_t4096", 4096, 2048, 1408, 60, 4, I_sh=5632),
     # tiny-layer shape at T=8192 with skewed (Zipf-like) expert popularity
-    "tiny_zipf_t8192": Workload("tiny_zipf_t8192", 8192, 256, 128, 8, 2),
+    "tiny_zipf_t8192": Workload("tiny_zipf_t8192", 8192, 256, 128, 8, 2, zipf=1.1),
 }
 
 
@@ -217,6 +230,8 @@ def draw_layer(wl: Workload, x_attempts: Optional[dict] = None) -> LayerInputs:
     s = wl.seed
     ex = draw_experts(s, wl.E, wl.H, wl.I)
     sh = draw_shared(s, wl.H, wl.I_sh, wl.gated_shared) if wl.I_sh else None
-    return LayerInputs(wl, draw_x(s, wl.T, wl.H, x_attempts),
-                       draw_residual(s + 1, wl.T, wl.H) if wl.residual else None,
-                       draw_router(s, wl.E, wl.H), ex, sh)
+    x = draw_x(s, wl.T, wl.H, x_attempts)
+    W_r = draw_router(s, wl.E, wl.H)
+    if wl.zipf > 0:
+        set_bias_channel(x, W_r, zipf_bias(wl.E, wl.zipf, wl.H))
+    return LayerInputs(wl, x, draw_residual(s + 1, wl.T, wl.H) if wl.residual else None, W_r, ex, sh)

@@ -28,3 +28,20 @@ def test_reference_arm_json_line():
     assert line["steps"] == 2 and line["warmup"] == 3
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_zipf_workload_is_skewed():
+    """The skewed-popularity workload (tiny layer shape, T=8192, Zipf(1.1) bias channel):
+    the bias channel survives margin redraws and expert popularity falls with the index."""
+    import numpy as np
+
+    import oracle
+    from mixture_experts_layer_09_gb300 import inputs as gen
+    import workloads as wk
+
+    inp = wk.layer("tiny_zipf_t8192")
+    assert np.all(inp.x[:, 0] == gen.ONE_BF16)
+    ids, _ = oracle.router_topk(oracle.router_logits(inp.x, inp.W_r), inp.wl.k)
+    share = np.bincount(ids.ravel(), minlength=inp.wl.E) / ids.size
+    assert share[0] > 0.3 and share[0] > 4 * share[-1]
+    assert np.all(np.diff(share[:4]) < 0)  # the head of the distribution is strictly ordered

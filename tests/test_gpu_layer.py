@@ -128,6 +128,13 @@ def test_layer_qwen15_prefill(moe, name, sample):
     _check_layer(moe, wk.layer(name), sample=sample)
 
 
+@pytest.mark.parametrize("arm", [1, 2])
+def test_layer_tiny_zipf_t8192(moe, arm):
+    """Tiny layer shape at T=8192 with Zipf(1.1)-skewed popularity (buckets from ~6,200 rows
+    down to ~400): the multi-CTA dispatch, many-tile experts and both arms, every token."""
+    _check_layer(moe, wk.layer("tiny_zipf_t8192"), arm=arm)
+
+
 def test_layer_qwen15_prefill_gemv_arm_agrees(moe):
     """Both arms on the same prefill batch: each within tolerance of the oracle."""
     inp = wk.layer("qwen15_prefill_t512", T=96)

@@ -35,6 +35,8 @@ def enforce_margin_x(inp: gen.LayerInputs, max_attempts: int = 64) -> gen.LayerI
             if a > max_attempts:
                 raise RuntimeError(f"token {t}: no margin after {max_attempts} redraws")
             inp.x[t] = gen.draw_x_row(wl.seed, t, wl.H, a)
+            if wl.zipf > 0:
+                inp.x[t, 0] = gen.ONE_BF16  # keep the bias channel
             logits[t] = oracle.router_logits(inp.x[t:t + 1], inp.W_r)[0]
         if a:
             attempts[t] = a
