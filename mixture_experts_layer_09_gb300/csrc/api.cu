@@ -88,7 +88,7 @@ void carve_gemm(Carver& c, int T, int k, int E, int H, int I, int I_sh, GemmBufs
     b.x16 = c.take<uint16_t>((R + Ts) * H);
     b.h16 = c.take<uint16_t>(R * I);
     b.sh_h16 = c.take<uint16_t>(Ts * (I_sh > 0 ? I_sh : 0));
-    b.tiles = c.take<int>(2 * static_cast<size_t>(gemm_ntile_max(static_cast<int>(R), E)));
+    b.tiles = c.take<int>(3 * static_cast<size_t>(gemm_ntile_max(static_cast<int>(R), E)));
     b.n_tiles = c.take<int>(1);
     b.rows = c.take<float>(R * H);
     b.sh_rows = c.take<float>(Ts * H);

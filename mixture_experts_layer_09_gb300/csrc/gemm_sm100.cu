@@ -1,31 +1,34 @@
 // gemm_sm100.cu -- tensor arm of the expert MLP (prefill batches): grouped GEMMs on the
 // 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
-// Each expert's bucket of dispatched rows is cut into tiles of up to 128 rows (daScript
-// PR #3988 "dasLLAMA vulkan: a MoE that fits the card ...", routed-block commit: the bucket
-// schedule places the buckets and their tiles; a tile with no rows returns at once).  A CTA
-// computes one (weight row block of 128, token tile) pair:
-//   A = 128 weight rows, int4 offset-binary with fp16 scales per 32 columns (colibri PR #418
-//       "Vulkan backend: expert tier + dense + MLA attention on any Vulkan 1.2 GPU",
-//       Correctness and "Grouped scales in the Vulkan kernels"), expanded by four producer
-//       warps into fp16 (nibble - 8) * scale directly in the 128-byte-swizzled K-major
-//       layout the tensor core reads;
-//   B = the tile's activation rows (fp16), brought in by TMA with the same swizzle;
-//   D = A * B^T in tensor memory (fp32), 128 lanes x N columns, N = tile rows rounded to 16.
-// Gate and up run as two accumulators of one CTA, so the epilogue forms silu(g) * u (the
-// fused gate+up+silu of colibri PR #418, Summary) and writes h in fp16.  The down GEMM's
-// epilogue writes either the unweighted rows (dispatch order), the rows weighted by their
-// top-k weight in slot order (the tensor arm's combine feed), or the shared expert's rows
-// scaled by sigmoid of its gate logit.
+// Each expert's bucket of dispatched rows is cut into token tiles of up to 256 rows, balanced
+// within the bucket (daScript PR #3988 "dasLLAMA vulkan: a MoE that fits the card ...",
+// routed-block commit: the bucket schedule places the buckets and their tiles).  The A operand
+// is int4 offset-binary weight rows with fp16 scales per 32 columns (colibri PR #418 "Vulkan
+// backend: expert tier + dense + MLA attention on any Vulkan 1.2 GPU", Correctness and
+// "Grouped scales in the Vulkan kernels"), expanded by producer warps into fp16
+// (nibble - 8) * scale directly in the 128-byte-swizzled K-major layout the tensor core
+// reads; B is the tile's activation rows (fp16), brought in by TMA with the same swizzle;
+// D = A * B^T accumulates in tensor memory (fp32), 128 lanes x N columns, N = tile rows
+// rounded to 16.
 //
-// Roles in a CTA of 576 threads: warp 0 issues the TMA loads of B, warp 1 owns the tensor
-// memory and issues the MMAs (one thread), warps 2-17 dequantise A (four threads per weight
-// row: with one CTA per SM the dequantisation is latency-bound, so more warps carry it) and
-// then run the epilogue (each warp one TMEM lane quadrant and a quarter of the columns).
+// Gate/up (moe_gateup_kernel): one CTA per (128 features, token tile); gate and up are two
+// accumulators of 256 columns, so the epilogue forms silu(g) * u (the fused gate+up+silu of
+// colibri PR #418, Summary) and writes h in fp16, staged in shared memory and stored one token
+// row per bulk copy.  Down (moe_down_kernel): persistent, one CTA per SM walking its work
+// items; two 256-column accumulators let one item's epilogue run during the next item's main
+// loop; the epilogue writes the unweighted rows (dispatch order), the rows weighted by their
+// top-k weight in slot order (the tensor arm's combine feed), or the shared expert's rows
+// scaled by sigmoid of its gate logit.  (The gate/up pair needs all 512 columns for one tile,
+// so it cannot double-buffer at this tile size; pairing 64 gate with 64 up rows would fit in
+// 256 columns but halves the work per pipeline stage, and measured slower.)
+//
 // Every mbarrier wait is bounded; a wait that runs out records MOE_ERR_DEVICE_TIMEOUT in the
-// status word, stops the CTA's loops, drains its own copies and MMAs, frees its tensor
-// memory and returns.
+// status word and every role of the CTA stops; the CTA drains its own copies and MMAs, frees
+// its tensor memory and returns.
 #include <cuda.h>
+
+#include <algorithm>
 
 #include "async.cuh"
 #include "tcgen05.cuh"
@@ -34,35 +37,48 @@
 
 namespace moe {
 
-constexpr int BM = 128;           // weight rows per tile (MMA M)
+constexpr int BM = 128;           // A rows per tile (MMA M)
 constexpr int BN = kGemmTileN;    // tokens per tile (MMA N upper bound)
+constexpr int BNB = 128;          // token rows per B TMA box
 constexpr int BK = 64;            // K per pipeline stage: 128 bytes of fp16 per row
 constexpr int kTileBytesA = BM * BK * 2;
 constexpr int kTileBytesB = BN * BK * 2;
-constexpr int kStagesGU = 3;
-constexpr int kStagesDN = 4;
-#ifndef MOE_GEMM_TPR
-#define MOE_GEMM_TPR 4
-#endif
-constexpr int kTpr = MOE_GEMM_TPR;              // dequantising threads per weight row
-constexpr int kCpt = 8 / kTpr;                  // 16-byte chunks (8 K-columns) per thread per K-step
-constexpr int kDqThreads = BM * kTpr;           // dequantising / epilogue threads (warps 2..)
-constexpr int kPrefetch = 4;                    // K-steps of raw weights in flight per thread
-constexpr int kGemmThreads = 64 + kDqThreads;   // + TMA warp + MMA warp
+static_assert(BN <= 256 && BN % BNB == 0, "one MMA per K-slice, whole TMA boxes");
+
+// gate/up kernel: 3 stages of (gate A, up A, B); 4 dequantising threads per A row
+constexpr int kGuStages = 3;
+constexpr int kGuStageBytes = 2 * kTileBytesA + kTileBytesB;
+constexpr int kGuTpr = 4;
+constexpr int kGuDqThreads = BM * kGuTpr;
+constexpr int kGuThreads = 64 + kGuDqThreads;
+constexpr int kGuPrefetch = 4;
+// down kernel: 4 stages of (A, B); 2 dequantising threads per A row; 4 epilogue warps
+constexpr int kDnStages = 4;
+constexpr int kDnStageBytes = kTileBytesA + kTileBytesB;
+constexpr int kDnTpr = 2;
+constexpr int kDnDqThreads = BM * kDnTpr;
+constexpr int kDnDqWarps = kDnDqThreads / 32;
+constexpr int kDnEpiWarp0 = 2 + kDnDqWarps;
+constexpr int kDnEpiThreads = 128;
+constexpr int kDnThreads = 64 + kDnDqThreads + kDnEpiThreads;
+constexpr int kDnPrefetch = 2;
+constexpr int kAccCols = 256;     // tensor-memory columns of one down accumulator
+constexpr int kEpiChunk = 32;     // down epilogue: token columns per tensor-memory load
+constexpr int kBarEpi = 3;        // named barrier of the down epilogue warps
 
 struct GemmK {
     CUtensorMap tm_r;     // B operand of routed tiles
     CUtensorMap tm_s;     // B operand of shared-expert tiles
     int T, k, E;
     int K_r, K_s;         // reduction length (H for gate/up, I or I_sh for down)
-    int M_r, M_s;         // weight rows (I or I_sh for gate/up, H for down)
-    int mblk_r, mblk_s;   // weight row blocks
-    int ctas_r;           // routed CTAs in the grid (ntile_max * mblk_r)
+    int M_r, M_s;         // output features (I or I_sh for gate/up, H for down)
+    int mblk_r, mblk_s;   // 128-row blocks of the output features
+    int items_r;          // routed work items (ntile_max * mblk_r); shared items follow
+    int items;            // all work items (the gate/up grid)
     int out_mode;         // down: 0 rows (unweighted, dispatch order), 1 weighted slots
     int sh_row0;          // B row of the first shared token in tm_s
-    const int* tiles;     // [2 * ntile] (expert, first dispatch row)
+    const int* tiles;     // [3 * ntile] (expert, first dispatch row, rows)
     const int* n_tiles;
-    const int32_t* offsets;
     const int32_t* perm;
     const float* topk_w;
     const float* sh_gate_logit;
@@ -82,6 +98,37 @@ struct GemmK {
     int* status;
 };
 
+struct Item {
+    bool shared;
+    int e, row0, nrows, mblk, K, M;
+};
+
+// Work item t: routed items first (tile-major, row blocks inner), then the shared expert's.
+// False when the item is past the tile schedule or has no rows (every role skips it alike).
+__device__ __forceinline__ bool item_at(const GemmK& p, int t, int n_tiles, Item& it) {
+    if (t < p.items_r) {
+        const int tix = t / p.mblk_r;
+        if (tix >= n_tiles) return false;
+        it.shared = false;
+        it.mblk = t % p.mblk_r;
+        it.e = __ldg(p.tiles + 3 * tix);
+        it.row0 = __ldg(p.tiles + 3 * tix + 1);
+        it.nrows = __ldg(p.tiles + 3 * tix + 2);
+        it.K = p.K_r;
+        it.M = p.M_r;
+    } else {
+        const int sid = t - p.items_r;
+        const int tix = sid / p.mblk_s;
+        it.shared = true;
+        it.mblk = sid % p.mblk_s;
+        it.e = -1;
+        it.row0 = tix * BN;
+        it.nrows = min(BN, p.T - it.row0);
+        it.K = p.K_s;
+        it.M = p.M_s;
+    }
+    return it.nrows > 0;
+}
 
 // 8 nibbles (columns 0..7 at bits 4c) times one fp16 scale -> 8 fp16 values, stored in the
 // K order [c0 c4 c1 c5 c2 c6 c3 c7] (the activations are stored in the same order, so the
@@ -108,94 +155,86 @@ __device__ __forceinline__ uint4 dequant8(uint32_t w, __half2 s2) {
 // Position of column c (0..7) of an 8-column group in that K order.
 __host__ __device__ constexpr inline int kperm8(int c) { return (c & 3) * 2 + (c >> 2); }
 
-// One K-step (64 columns) of a thread's part of a weight row: kCpt words of nibbles (8 columns
-// each) and the scale of their group (a part never straddles two 32-column groups).
+// One K-step (64 columns) of a thread's part of a weight row: CPT words of nibbles (8 columns
+// each, CPT = 8 / threads per row) and the scale of their 32-column group.
+template <int CPT>
 struct RawK {
-    uint32_t q[kCpt];
+    uint32_t q[CPT];
     uint16_t s;
 };
 
-__device__ __forceinline__ RawK load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, int part, bool valid) {
-    RawK r;
+template <int CPT>
+__device__ __forceinline__ RawK<CPT> load_raw(const uint8_t* qrow, const uint16_t* srow, int kb, int part, bool valid) {
+    static_assert(CPT == 2 || CPT == 4, "a part stays inside one 32-column scale group");
+    RawK<CPT> r;
     if (valid) {
-        const uint8_t* src = qrow + kb * 32 + part * kCpt * 4;
-        if constexpr (kCpt == 4) {
+        const uint8_t* src = qrow + kb * 32 + part * CPT * 4;
+        if constexpr (CPT == 4) {
             const uint4 v = ldg_nc(src);
             r.q[0] = v.x; r.q[1] = v.y; r.q[2] = v.z; r.q[3] = v.w;
         } else {
             const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
             r.q[0] = v.x; r.q[1] = v.y;
         }
-        r.s = __ldg(srow + kb * 2 + (part * kCpt) / 4);
+        r.s = __ldg(srow + kb * 2 + (part * CPT) / 4);
     } else {
 #pragma unroll
-        for (int j = 0; j < kCpt; ++j) r.q[j] = 0x88888888u;  // all zero weights
+        for (int j = 0; j < CPT; ++j) r.q[j] = 0x88888888u;  // all zero weights
         r.s = 0;
     }
     return r;
 }
 
-// Writes chunks part*kCpt .. part*kCpt+kCpt-1 of `row` into a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int part, const RawK& r) {
+// Writes chunks part*CPT .. part*CPT+CPT-1 of `row` into a 128-byte-swizzled K-major tile.
+template <int CPT>
+__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int part, const RawK<CPT>& r) {
     const __half2 s2 = __half2half2(__ushort_as_half(r.s));
     uint8_t* rowp = tile + row * 128;
 #pragma unroll
-    for (int j = 0; j < kCpt; ++j) {
-        const int c = part * kCpt + j;
+    for (int j = 0; j < CPT; ++j) {
+        const int c = part * CPT + j;
         *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = dequant8(r.q[j], s2);
     }
 }
 
-template <int MODE>  // 0 = gate+up (two accumulators, SwiGLU epilogue), 1 = down
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmK p) {
+// TMA of a tile's B rows for one K-step: one 128-row box per lane (copies issued by one thread
+// are served one after another), only the boxes that hold tile rows.  Called by a whole warp.
+__device__ __forceinline__ void load_b_stage(uint8_t* dst, const CUtensorMap* tm, int kb, int brow, int nrows,
+                                             uint64_t* bar, int lane) {
+    const int nbox = (nrows + BNB - 1) / BNB;
+    if (lane == 0) mbar_arrive_expect_tx(bar, nbox * BNB * BK * 2);
+    __syncwarp();
+    if (lane < nbox) tma_load_2d(dst + lane * BNB * 128, tm, kb * BK, brow + lane * BNB, bar);
+}
+
+// ------------------------------------------------------------------ gate + up (+ SwiGLU)
+// One CTA per work item (128 features, token tile).  Warp 0 issues the TMA loads of B, warp 1
+// owns the tensor memory and issues the MMAs (one thread), warps 2-17 dequantise the gate and
+// up rows (four threads per row) and then run the epilogue (each warp one tensor-memory lane
+// quadrant and a quarter of the token columns).
+__global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_constant__ GemmK p) {
     pdl_wait();
     pdl_trigger();
-    constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
-    constexpr int NMAT = MODE == 0 ? 2 : 1;
-    constexpr int kStageBytes = NMAT * kTileBytesA + kTileBytesB;
-    constexpr uint32_t kTmemCols = MODE == 0 ? 2 * BN : BN;
-
-    // ---- which tile this CTA computes
-    const bool shared = static_cast<int>(blockIdx.x) >= p.ctas_r;
-    int e, row0, nrows, mblk, K, M;
-    if (!shared) {
-        const int tix = blockIdx.x / p.mblk_r;
-        mblk = blockIdx.x % p.mblk_r;
-        if (tix >= *p.n_tiles) return;  // tile beyond the schedule: nothing to do
-        e = p.tiles[2 * tix];
-        row0 = p.tiles[2 * tix + 1];
-        nrows = min(BN, p.offsets[e + 1] - row0);
-        K = p.K_r;
-        M = p.M_r;
-    } else {
-        const int sid = blockIdx.x - p.ctas_r;
-        const int tix = sid / p.mblk_s;
-        mblk = sid % p.mblk_s;
-        e = -1;
-        row0 = tix * BN;
-        nrows = min(BN, p.T - row0);
-        K = p.K_s;
-        M = p.M_s;
-    }
-    if (nrows <= 0) return;
-    const int nk = K / BK;
+    constexpr int S = kGuStages;
+    constexpr int CPT = 8 / kGuTpr;
+    Item w;
+    if (!item_at(p, blockIdx.x, __ldg(p.n_tiles), w)) return;  // no rows: nothing to do
+    const int nk = w.K / BK;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + S * kGuStageBytes);
     uint64_t* full_b = full_a + S;
     uint64_t* empty = full_b + S;
     uint64_t* accum = empty + S;
     uint64_t* drain = accum + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* row_slot = const_cast<int*>(abort_flag) + 1;           // [BN] down: slot of each tile row
-    float* row_w = reinterpret_cast<float*>(row_slot + BN);     // [BN] down: its weight / shared gate
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            mbar_init(full_a + s, kDqThreads / 32);  // one arrival per dequantising warp
+            mbar_init(full_a + s, kGuDqThreads / 32);  // one arrival per dequantising warp
             mbar_init(full_b + s, 1);
             mbar_init(empty + s, 1);
         }
@@ -204,42 +243,40 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == 1) tmem_alloc(tmem_slot, 2 * BN);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto stage_a = [&](int s, int mat) { return smem + s * kStageBytes + mat * kTileBytesA; };
-    auto stage_b = [&](int s) { return smem + s * kStageBytes + NMAT * kTileBytesA; };
+    auto stage_a = [&](int s, int mat) { return smem + s * kGuStageBytes + mat * kTileBytesA; };
+    auto stage_b = [&](int s) { return smem + s * kGuStageBytes + 2 * kTileBytesA; };
 
     if (warp == 0) {
         // ---------------- TMA producer of B
-        if (lane == 0) {
-            const CUtensorMap* tm = shared ? &p.tm_s : &p.tm_r;
-            const int brow = shared ? p.sh_row0 + row0 : row0;
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % S;
-                if (kb >= S && !mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 1)) break;
-                mbar_arrive_expect_tx(full_b + s, kTileBytesB);
-                tma_load_2d(stage_b(s), tm, kb * BK, brow, full_b + s);
-                issued = kb + 1;
-            }
-            if (*abort_flag) {
-                // let the copies this thread started land before the CTA leaves
-                for (int kb = max(0, issued - S); kb < issued; ++kb) {
-                    const long long t0 = clock64();
-                    while (!mbar_try_wait(full_b + kb % S, (kb / S) & 1) && clock64() - t0 < kWaitLimitCycles) {
-                    }
+        const CUtensorMap* tm = w.shared ? &p.tm_s : &p.tm_r;
+        const int brow = w.shared ? p.sh_row0 + w.row0 : w.row0;
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % S;
+            bool ok = true;
+            if (kb >= S && lane == 0) ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 1);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            load_b_stage(stage_b(s), tm, kb, brow, w.nrows, full_b + s, lane);
+            issued = kb + 1;
+        }
+        if (*abort_flag && lane == 0) {
+            // let the copies this warp started land before the CTA leaves
+            for (int kb = max(0, issued - S); kb < issued; ++kb) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(full_b + kb % S, (kb / S) & 1) && clock64() - t0 < kWaitLimitCycles) {
                 }
             }
         }
     } else if (warp == 1) {
-        // ---------------- MMA issuer
+        // ---------------- MMA issuer: gate into columns 0.., up into columns BN..
         if (lane == 0) {
-            const int nmma = (nrows + 15) & ~15;
-            const uint32_t idesc = idesc_f16_m128(nmma);
+            const uint32_t idesc = idesc_f16_m128((w.nrows + 15) & ~15);
             bool any = false;
             for (int kb = 0; kb < nk; ++kb) {
                 const int s = kb % S;
@@ -253,10 +290,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                     const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
                     const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
 #pragma unroll
-                    for (int mat = 0; mat < NMAT; ++mat) {
-                        const uint64_t ad = sw128_kmajor_desc(smem_u32(stage_a(s, mat)) + kk * 32);
-                        mma_f16(tmem + mat * BN, ad, bd, idesc, acc);
-                    }
+                    for (int mat = 0; mat < 2; ++mat)
+                        mma_f16(tmem + mat * BN, sw128_kmajor_desc(smem_u32(stage_a(s, mat)) + kk * 32), bd, idesc, acc);
                 }
                 mma_commit(empty + s);
                 any = true;
@@ -271,49 +306,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             }
         }
     } else {
-        // ---------------- A producers (8 warps: two threads per weight row), then the epilogue
+        // ---------------- gate and up producers (kGuTpr threads per feature), then the epilogue
         const int dt = threadIdx.x - 64;
-        const int pr = dt / kTpr, half = dt % kTpr;  // weight row within the block, part of its K-step
-        const int wrow = mblk * BM + pr;        // weight row within the matrix
-        const bool valid = wrow < M;
-        const size_t grow = shared ? static_cast<size_t>(wrow) : static_cast<size_t>(e) * M + wrow;
-        const uint8_t* qa = (shared ? p.qa_s : p.qa_r) + grow * (K / 2);
-        const uint16_t* sa = (shared ? p.sa_s : p.sa_r) + grow * (K / 32);
-        const uint8_t* qb = nullptr;
-        const uint16_t* sb = nullptr;
-        if (MODE == 0) {
-            qb = (shared ? p.qb_s : p.qb_r) + grow * (K / 2);
-            sb = (shared ? p.sb_s : p.sb_r) + grow * (K / 32);
-        }
-        if (MODE == 1) {
-            // the epilogue's per-row data, loaded now so it is not on the epilogue's path
-            if (dt < nrows) {
-                const int r = row0 + dt;
-                if (shared) {
-                    float gate = 1.f;
-                    if (p.sh_gate_logit) gate = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
-                    row_slot[dt] = r;
-                    row_w[dt] = gate;
-                } else if (p.out_mode == 1) {  // weighted slot rows; rows mode needs no table
-                    const int a = __ldg(p.perm + r);
-                    row_slot[dt] = a;
-                    row_w[dt] = __ldg(p.topk_w + a);
-                }
-            }
-        }
-        // raw weights kPrefetch K-steps ahead in registers; one lane per warp waits for a free
-        // stage and one arrives for the warp (after __syncwarp orders the warp's writes), so
-        // that 256 threads do not poll and arrive on one barrier word every K-step
-        RawK ra[kPrefetch], rb[kPrefetch];
+        const int pr = dt / kGuTpr, part = dt % kGuTpr;  // feature within the block, part of its K-step
+        const int f = w.mblk * BM + pr;
+        const bool valid = f < w.M;
+        const size_t grow = w.shared ? static_cast<size_t>(f) : static_cast<size_t>(w.e) * w.M + f;
+        const uint8_t* qa = (w.shared ? p.qa_s : p.qa_r) + grow * (w.K / 2);
+        const uint16_t* sa = (w.shared ? p.sa_s : p.sa_r) + grow * (w.K / 32);
+        const uint8_t* qb = (w.shared ? p.qb_s : p.qb_r) + grow * (w.K / 2);
+        const uint16_t* sb = (w.shared ? p.sb_s : p.sb_r) + grow * (w.K / 32);
+        // raw weights kGuPrefetch K-steps ahead in registers; one lane per warp waits for a free
+        // stage and one arrives for the warp (after __syncwarp orders the warp's writes)
+        RawK<CPT> ra[kGuPrefetch], rb[kGuPrefetch];
 #pragma unroll
-        for (int d = 0; d < kPrefetch; ++d) {
-            ra[d] = load_raw(qa, sa, d, half, valid && d < nk);
-            if (MODE == 0) rb[d] = load_raw(qb, sb, d, half, valid && d < nk);
+        for (int d = 0; d < kGuPrefetch; ++d) {
+            ra[d] = load_raw<CPT>(qa, sa, d, part, valid && d < nk);
+            rb[d] = load_raw<CPT>(qb, sb, d, part, valid && d < nk);
         }
         bool ok = true;
-        for (int kb0 = 0; kb0 < nk && ok; kb0 += kPrefetch) {
+        for (int kb0 = 0; kb0 < nk && ok; kb0 += kGuPrefetch) {
 #pragma unroll
-            for (int d = 0; d < kPrefetch; ++d) {
+            for (int d = 0; d < kGuPrefetch; ++d) {
                 const int kb = kb0 + d;
                 if (kb >= nk) break;
                 const int s = kb % S;
@@ -325,75 +339,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                         break;
                     }
                 }
-                store_dequant(stage_a(s, 0), pr, half, ra[d]);
-                if (MODE == 0) store_dequant(stage_a(s, 1), pr, half, rb[d]);
+                store_dequant<CPT>(stage_a(s, 0), pr, part, ra[d]);
+                store_dequant<CPT>(stage_a(s, 1), pr, part, rb[d]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a + s);
-                if (kb + kPrefetch < nk) {
-                    ra[d] = load_raw(qa, sa, kb + kPrefetch, half, valid);
-                    if (MODE == 0) rb[d] = load_raw(qb, sb, kb + kPrefetch, half, valid);
+                if (kb + kGuPrefetch < nk) {
+                    ra[d] = load_raw<CPT>(qa, sa, kb + kGuPrefetch, part, valid);
+                    rb[d] = load_raw<CPT>(qb, sb, kb + kGuPrefetch, part, valid);
                 }
             }
         }
-        named_barrier(2, kDqThreads);  // row_slot / row_w visible to every epilogue thread
-        // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp)
-        // The tile is staged in the pipeline's shared memory (free once the accumulators are
-        // final): row c = token row of the tile, 128 output columns; then each thread writes
-        // one token row with a bulk copy.  Gate/up stage fp16 h in the down GEMM's K order,
-        // down stages fp32 (weighted) outputs bound for the row's slot or token.
+        // ---------------- epilogue (tcgen05.ld is warp-collective: decide per warp).  The tile
+        // is staged in the pipeline's shared memory (free once the accumulators are final) as
+        // fp16 h in the down GEMM's K order, then each thread writes one token row by bulk copy.
         bool go = __all_sync(0xffffffffu, ok);
         if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5));
-        go = named_barrier_or(2, kDqThreads, !go) ? false : go;  // all epilogue warps agree
+        go = named_barrier_or(2, kGuDqThreads, !go) ? false : go;  // all epilogue warps agree
         if (go) {
             tc_fence_after();
             const int q = warp & 3;                 // tensor-memory lane quadrant of this warp
-            const int m = q * 32 + lane;            // accumulator row = weight row in the block
+            const int m = q * 32 + lane;            // accumulator row = feature in the block
             const int ch = (warp - 2) >> 2;         // column share handled by this warp
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            constexpr int kCols = BN / (kDqThreads / 128);
-            const int cbeg = ch * kCols, cend = min(nrows, cbeg + kCols);
-            if (MODE == 0) {
-                uint16_t* stile = reinterpret_cast<uint16_t*>(smem);           // [BN][BM] fp16
-                const int pos = (m & ~7) + kperm8(m & 7);                     // K order of the down GEMM
-                for (int c0 = cbeg; c0 < cend; c0 += 32) {
-                    float g[32], u[32];
-                    tmem_ld32x2(tbase + c0, tbase + BN + c0, g, u);
+            constexpr int kCols = BN / (kGuDqThreads / 128);
+            const int cbeg = ch * kCols, cend = min(w.nrows, cbeg + kCols);
+            uint16_t* stile = reinterpret_cast<uint16_t*>(smem);  // [BN][BM] fp16
+            const int pos = (m & ~7) + kperm8(m & 7);
+            for (int c0 = cbeg; c0 < cend; c0 += 32) {
+                float g[32], u[32];
+                tmem_ld32x2(tbase + c0, tbase + BN + c0, g, u);
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        if (c0 + cc < cend) {
-                            const float h = __fdividef(g[cc] * u[cc], 1.f + __expf(-g[cc]));
-                            stile[(c0 + cc) * BM + pos] = __half_as_ushort(__float2half_rn(h));
-                        }
-                    }
-                }
-            } else {
-                float* stile = reinterpret_cast<float*>(smem);                 // [BN][BM] fp32
-                const bool weighted = shared || p.out_mode == 1;
-                for (int c0 = cbeg; c0 < cend; c0 += 32) {
-                    float d[32];
-                    tmem_ld32(tbase + c0, d);
-#pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        if (c0 + cc < cend) stile[(c0 + cc) * BM + m] = weighted ? row_w[c0 + cc] * d[cc] : d[cc];
+                for (int cc = 0; cc < 32; ++cc) {
+                    if (c0 + cc < cend) {
+                        const float h = __fdividef(g[cc] * u[cc], 1.f + __expf(-g[cc]));
+                        stile[(c0 + cc) * BM + pos] = __half_as_ushort(__float2half_rn(h));
                     }
                 }
             }
             fence_proxy_async_smem();  // the tile's generic writes, before the bulk copies read it
-            named_barrier(2, kDqThreads);
-            if (dt < nrows) {
-                const int cols = min(BM, M - mblk * BM);
-                if (MODE == 0) {
-                    uint16_t* hout = shared ? p.h_s : p.h_r;
-                    bulk_store(hout + static_cast<size_t>(row0 + dt) * M + mblk * BM,
-                               reinterpret_cast<const uint16_t*>(smem) + dt * BM, cols * 2);
-                } else {
-                    const size_t orow = shared ? static_cast<size_t>(row0 + dt)
-                                               : (p.out_mode == 1 ? static_cast<size_t>(row_slot[dt])
-                                                                  : static_cast<size_t>(row0 + dt));
-                    float* out = shared ? p.out_s : p.out_r;
-                    bulk_store(out + orow * M + mblk * BM, reinterpret_cast<const float*>(smem) + dt * BM, cols * 4);
-                }
+            named_barrier(2, kGuDqThreads);
+            if (dt < w.nrows) {
+                const int cols = min(BM, w.M - w.mblk * BM);
+                uint16_t* hout = w.shared ? p.h_s : p.h_r;
+                bulk_store(hout + static_cast<size_t>(w.row0 + dt) * w.M + w.mblk * BM, stile + dt * BM, cols * 2);
                 bulk_store_wait();
             }
         }
@@ -402,12 +391,241 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, 2 * BN);
+    }
+}
+
+// ------------------------------------------------------------------ down (persistent)
+// One CTA per SM walks work items blockIdx.x, + gridDim.x, ...; item n accumulates into
+// tensor-memory buffer n & 1.  Warp 0 issues the TMA loads of B; warp 1 owns the tensor memory
+// and issues the MMAs (one thread); warps 2-9 dequantise A (two threads per row); warps 10-13
+// run the epilogue, one tensor-memory lane quadrant each, storing straight from registers (a
+// warp's 32 lanes are 32 consecutive output columns of one token row).
+__global__ void __launch_bounds__(kDnThreads, 1) moe_down_kernel(const __grid_constant__ GemmK p) {
+    pdl_wait();
+    pdl_trigger();
+    constexpr int S = kDnStages;
+    constexpr int CPT = 8 / kDnTpr;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + S * kDnStageBytes);
+    uint64_t* full_b = full_a + S;
+    uint64_t* empty = full_b + S;
+    uint64_t* tfull = empty + S;   // [2] accumulator ready for the epilogue
+    uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
+    uint64_t* drain = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* row_out = const_cast<int*>(abort_flag) + 1;            // [2][BN] output row of each tile row
+    float* row_w = reinterpret_cast<float*>(row_out + 2 * BN);  // [2][BN] its weight / shared gate
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_a + s, kDnDqWarps);  // one arrival per dequantising warp
+            mbar_init(full_b + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull + b, 1);
+            mbar_init(tempty + b, kDnEpiThreads / 32);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, 2 * kAccCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int n_tiles = __ldg(p.n_tiles);
+
+    auto stage_a = [&](int s) { return smem + s * kDnStageBytes; };
+    auto stage_b = [&](int s) { return smem + s * kDnStageBytes + kTileBytesA; };
+
+    if (warp == 0) {
+        // ---------------- TMA producer of B
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.items && ok; t += gridDim.x) {
+            Item w;
+            if (!item_at(p, t, n_tiles, w)) continue;
+            const CUtensorMap* tm = w.shared ? &p.tm_s : &p.tm_r;
+            const int brow = w.shared ? p.sh_row0 + w.row0 : w.row0;
+            const int nk = w.K / BK;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = it % S;
+                if (it >= S && lane == 0) ok = mbar_wait(empty + s, ((it / S) & 1) ^ 1, abort_flag, p.status, 1);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                load_b_stage(stage_b(s), tm, kb, brow, w.nrows, full_b + s, lane);
+                ++it;
+            }
+        }
+        if (*abort_flag && lane == 0) {
+            // let the copies this warp started land before the CTA leaves
+            for (uint32_t j = it > static_cast<uint32_t>(S) ? it - S : 0; j < it; ++j) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(full_b + j % S, (j / S) & 1) && clock64() - t0 < kWaitLimitCycles) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            uint32_t it = 0, n = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < p.items && ok; t += gridDim.x) {
+                Item w;
+                if (!item_at(p, t, n_tiles, w)) continue;
+                const int b = n & 1;
+                if (n >= 2 && !mbar_wait(tempty + b, ((n >> 1) & 1) ^ 1, abort_flag, p.status, 6)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t idesc = idesc_f16_m128((w.nrows + 15) & ~15);
+                const uint32_t dacc = tmem + b * kAccCols;
+                const int nk = w.K / BK;
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = it % S;
+                    const uint32_t par = (it / S) & 1;
+                    if (!mbar_wait(full_b + s, par, abort_flag, p.status, 2) ||
+                        !mbar_wait(full_a + s, par, abort_flag, p.status, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(stage_a(s)), b0 = smem_u32(stage_b(s));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_f16(dacc, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                                (kb > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(empty + s);
+                    any = true;
+                    ++it;
+                }
+                if (!ok) break;
+                mma_commit(tfull + b);
+                ++n;
+            }
+            if (*abort_flag && any) {
+                mma_commit(drain);  // wait for this thread's MMAs before tensor memory is freed
+                const long long t0 = clock64();
+                while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+                }
+            }
+        }
+    } else if (warp < kDnEpiWarp0) {
+        // ---------------- A producers (kDnTpr threads per row of W_d)
+        const int dt = threadIdx.x - 64;
+        const int pr = dt / kDnTpr, part = dt % kDnTpr;  // A row of the item, part of its K-step
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.items && ok; t += gridDim.x) {
+            Item w;
+            if (!item_at(p, t, n_tiles, w)) continue;
+            const int wrow = w.mblk * BM + pr;
+            const bool valid = wrow < w.M;
+            const size_t grow = w.shared ? static_cast<size_t>(wrow) : static_cast<size_t>(w.e) * w.M + wrow;
+            const uint8_t* qa = (w.shared ? p.qa_s : p.qa_r) + grow * (w.K / 2);
+            const uint16_t* sa = (w.shared ? p.sa_s : p.sa_r) + grow * (w.K / 32);
+            const int nk = w.K / BK;
+            // raw weights kDnPrefetch K-steps ahead in registers; one lane per warp waits for a
+            // free stage and one arrives for the warp (after __syncwarp orders its writes)
+            RawK<CPT> ra[kDnPrefetch];
+#pragma unroll
+            for (int d = 0; d < kDnPrefetch; ++d) ra[d] = load_raw<CPT>(qa, sa, d, part, valid && d < nk);
+            for (int kb0 = 0; kb0 < nk && ok; kb0 += kDnPrefetch) {
+#pragma unroll
+                for (int d = 0; d < kDnPrefetch; ++d) {
+                    const int kb = kb0 + d;
+                    if (kb >= nk) break;
+                    const int s = it % S;
+                    if (it >= S) {
+                        bool free_ok = true;
+                        if (lane == 0) free_ok = mbar_wait(empty + s, ((it / S) & 1) ^ 1, abort_flag, p.status, 4);
+                        if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    store_dequant<CPT>(stage_a(s), pr, part, ra[d]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full_a + s);
+                    if (kb + kDnPrefetch < nk) ra[d] = load_raw<CPT>(qa, sa, kb + kDnPrefetch, part, valid);
+                    ++it;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue: warp q = warp & 3 reads tensor-memory lanes 32q .. 32q+31
+        const int et = threadIdx.x - 64 - kDnDqThreads;
+        const int q = warp & 3, m = q * 32 + lane;
+        uint32_t n = 0;
+        for (int t = blockIdx.x; t < p.items; t += gridDim.x) {
+            Item w;
+            if (!item_at(p, t, n_tiles, w)) continue;
+            const int b = n & 1;
+            int* ro = row_out + b * BN;
+            float* rw = row_w + b * BN;
+            // the tile's output rows and weights, while the main loop runs (two copies: the
+            // previous item's may still be in use by a slower epilogue warp)
+            for (int i = et; i < w.nrows; i += kDnEpiThreads) {
+                const int r = w.row0 + i;
+                if (w.shared) {
+                    float gate = 1.f;
+                    if (p.sh_gate_logit)
+                        gate = 1.f / (1.f + expf(-__ldg(p.sh_gate_logit + static_cast<size_t>(r) * p.logit_ld)));
+                    ro[i] = r;
+                    rw[i] = gate;
+                } else if (p.out_mode == 1) {
+                    const int a = __ldg(p.perm + r);
+                    ro[i] = a;
+                    rw[i] = __ldg(p.topk_w + a);
+                } else {
+                    ro[i] = r;
+                    rw[i] = 1.f;
+                }
+            }
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(tfull + b, (n >> 1) & 1, abort_flag, p.status, 5);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (named_barrier_or(kBarEpi, kDnEpiThreads, !ok)) break;  // every epilogue warp stops alike
+            tc_fence_after();
+            const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols;
+            const int col = w.mblk * BM + m;
+            float* out = w.shared ? p.out_s : p.out_r;
+            for (int c0 = 0; c0 < w.nrows; c0 += kEpiChunk) {
+                const int nc = min(kEpiChunk, w.nrows - c0);
+                float d[32];
+                tmem_ld32(tb + c0, d);
+                if (col < w.M) {
+#pragma unroll
+                    for (int cc = 0; cc < 32; ++cc)
+                        if (cc < nc) out[static_cast<size_t>(ro[c0 + cc]) * w.M + col] = rw[c0 + cc] * d[cc];
+                }
+            }
+            tc_fence_before();  // this warp's tensor-memory reads, before the buffer is handed back
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty + b);
+            ++n;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 2 * kAccCols);
     }
 }
 
 // ------------------------------------------------------------------ small helpers
-// Tile list from the bucket offsets: tiles of up to BN rows per expert, expert-major.
+// Tile list from the bucket offsets, expert-major: a bucket of c rows takes ceil(c / BN) tiles
+// of ceil(c / tiles) rows each (the last one may be shorter), so that no tile is a short tail
+// that pays a whole pass over the expert's weights for a few rows.
 __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restrict__ offsets, int E,
                                                           int* __restrict__ tiles, int* __restrict__ n_tiles) {
     pdl_wait();
@@ -416,6 +634,7 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     const int e = threadIdx.x, lane = e & 31, w = e >> 5;
     const int cnt = (e < E) ? offsets[e + 1] - offsets[e] : 0;
     const int nt = (cnt + BN - 1) / BN;
+    const int per = nt > 0 ? (cnt + nt - 1) / nt : 0;
     int incl = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -428,8 +647,9 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
     for (int i = 0; i < w; ++i) base += warp_tot[i];
     if (e == 255) *n_tiles = base + nt;
     for (int j = 0; j < nt; ++j) {
-        tiles[2 * (base + j)] = e;
-        tiles[2 * (base + j) + 1] = offsets[e] + j * BN;
+        tiles[3 * (base + j)] = e;
+        tiles[3 * (base + j) + 1] = offsets[e] + j * per;
+        tiles[3 * (base + j) + 2] = max(0, min(per, cnt - j * per));
     }
 }
 
@@ -467,7 +687,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __rest
 // 2D fp16 tensor [rows][K], box = 64 x BN, 128-byte swizzle, zero fill outside.
 static bool make_tmap(CUtensorMap* m, const void* base, int K, int rows) {
     return tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, static_cast<uint64_t>(K), static_cast<uint64_t>(rows),
-                   static_cast<uint64_t>(K) * 2, BK, BN, CU_TENSOR_MAP_SWIZZLE_128B);
+                   static_cast<uint64_t>(K) * 2, BK, BNB, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 int gemm_ntile_max(int n_slots, int E) { return (n_slots + BN - 1) / BN + E; }
@@ -476,17 +696,31 @@ bool gemm_supported(int H, int I, int I_sh) {
     return H % BK == 0 && I % BK == 0 && (I_sh <= 0 || I_sh % BK == 0);
 }
 
-template <int MODE>
-static size_t gemm_smem_bytes() {
-    constexpr int S = MODE == 0 ? kStagesGU : kStagesDN;
-    constexpr int NMAT = MODE == 0 ? 2 : 1;
-    return static_cast<size_t>(S) * (NMAT * kTileBytesA + kTileBytesB) + 1024 + 256 + 8 * BN;
+static size_t gateup_smem_bytes() { return 1024 + static_cast<size_t>(kGuStages) * kGuStageBytes + 256; }
+
+static size_t down_smem_bytes() {
+    // stages | barriers, tensor-memory slot, abort flag | two row tables
+    return 1024 + static_cast<size_t>(kDnStages) * kDnStageBytes + 256 + 2 * BN * 8;
 }
 
-template <int MODE>
-static cudaError_t set_smem_attr() {
-    static cudaError_t once = cudaFuncSetAttribute(moe_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(gemm_smem_bytes<MODE>()));
+static int sm_count() {
+    static int n = [] {
+        int dev = 0, v = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        return v > 0 ? v : 148;
+    }();
+    return n;
+}
+
+static cudaError_t set_smem_attrs() {
+    static cudaError_t once = [] {
+        cudaError_t e = cudaFuncSetAttribute(moe_gateup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(gateup_smem_bytes()));
+        if (e != cudaSuccess) return e;
+        return cudaFuncSetAttribute(moe_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(down_smem_bytes()));
+    }();
     return once;
 }
 
@@ -494,8 +728,7 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     cudaError_t err;
     const int n_slots = p.T * p.k;
     const bool has_sh = p.sh_I > 0;
-    if ((err = set_smem_attr<0>()) != cudaSuccess) return err;
-    if ((err = set_smem_attr<1>()) != cudaSuccess) return err;
+    if ((err = set_smem_attrs()) != cudaSuccess) return err;
     // 1. activations in dispatch order (and token order for the shared expert), fp16
     {
         const long total = static_cast<long>(n_slots + (has_sh ? p.T : 0)) * (p.H / 8);
@@ -524,7 +757,6 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     g.E = p.E;
     g.tiles = p.tiles;
     g.n_tiles = p.n_tiles;
-    g.offsets = p.offsets;
     g.perm = p.perm;
     g.topk_w = p.topk_w;
     g.sh_gate_logit = p.sh_gate_logit;
@@ -536,7 +768,8 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     g.M_s = has_sh ? p.sh_I : BM;
     g.mblk_r = (p.I + BM - 1) / BM;
     g.mblk_s = has_sh ? (p.sh_I + BM - 1) / BM : 1;
-    g.ctas_r = p.ntile_max * g.mblk_r;
+    g.items_r = p.ntile_max * g.mblk_r;
+    g.items = g.items_r + (has_sh ? p.sh_tiles * g.mblk_s : 0);
     g.sh_row0 = n_slots;
     if (!make_tmap(&g.tm_r, p.x16, p.H, n_slots + (has_sh ? p.T : 0))) return cudaErrorInvalidValue;
     g.tm_s = g.tm_r;
@@ -551,11 +784,8 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     g.h_r = p.h16;
     g.h_s = p.sh_h16;
     {
-        const int ctas = g.ctas_r + (has_sh ? p.sh_tiles * g.mblk_s : 0);
-        {
-            KernelScope ks_("gemm_gateup", st);
-            err = launch_pdl(moe_gemm_kernel<0>, dim3(ctas), dim3(kGemmThreads), gemm_smem_bytes<0>(), st, g);
-        }
+        KernelScope ks_("gemm_gateup", st);
+        err = launch_pdl(moe_gateup_kernel, dim3(g.items), dim3(kGuThreads), gateup_smem_bytes(), st, g);
         if (err != cudaSuccess) return err;
     }
     // 4. down (+ weighting / shared gate in the epilogue)
@@ -566,7 +796,8 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     d.M_s = p.H;
     d.mblk_r = (p.H + BM - 1) / BM;
     d.mblk_s = d.mblk_r;
-    d.ctas_r = p.ntile_max * d.mblk_r;
+    d.items_r = p.ntile_max * d.mblk_r;
+    d.items = d.items_r + (has_sh ? p.sh_tiles * d.mblk_s : 0);
     d.sh_row0 = 0;
     d.out_mode = rows_mode ? 0 : 1;
     if (!make_tmap(&d.tm_r, p.h16, p.I, n_slots)) return cudaErrorInvalidValue;
@@ -586,11 +817,9 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     d.out_r = rows_mode ? p.rows_out : p.slot_out;
     d.out_s = p.sh_out;
     {
-        const int ctas = d.ctas_r + (has_sh ? p.sh_tiles * d.mblk_s : 0);
-        {
-            KernelScope ks_("gemm_down", st);
-            err = launch_pdl(moe_gemm_kernel<1>, dim3(ctas), dim3(kGemmThreads), gemm_smem_bytes<1>(), st, d);
-        }
+        KernelScope ks_("gemm_down", st);
+        err = launch_pdl(moe_down_kernel, dim3(std::min(d.items, sm_count())), dim3(kDnThreads), down_smem_bytes(),
+                         st, d);
         if (err != cudaSuccess) return err;
     }
     return cudaSuccess;

@@ -150,7 +150,7 @@ struct GemmPlan {
     uint16_t* x16;                // fp16 [T*k + T][H]: dispatch-order rows, then token-order rows
     uint16_t* h16;                // fp16 [T*k][I]
     uint16_t* sh_h16;             // fp16 [T][I_sh]
-    int* tiles;                   // [ntile_max] packed (expert, row start, rows)
+    int* tiles;                   // [3 * ntile_max] (expert, row start, rows)
     int* n_tiles;
     int* status;
     // outputs
