@@ -5,8 +5,9 @@
 // the gate logit is one more router row past the router's logits).  A CTA takes 128 tokens
 // (MMA M = 128) and all E (+1) router rows (MMA N, rounded up to 16, split at 256): bf16 A and
 // B in 128-byte-swizzled K-major tiles, fp32 accumulators in tensor memory.  Warp 0 brings the
-// token tile and the router rows by TMA and writes the gate row into the B tile itself; warp 1
-// issues the MMAs; warps 2-5 read the accumulators and store the logits.  Waits are bounded.
+// token tile (two boxes) and the router rows by TMA, one copy per lane, and writes the gate row
+// into the B tile itself; warp 1 issues the MMAs; warps 2-5 read the accumulators and store the
+// logits.  Waits are bounded.
 #include <cuda.h>
 
 #include <algorithm>
@@ -27,7 +28,7 @@ constexpr int kSmemBudget = 227 * 1024;
 static_assert(kTileA % 1024 == 0, "swizzled tiles stay 1024-aligned");
 
 struct RouterTcArgs {
-    CUtensorMap tm_x;   // bf16 [T][H], box 64 x 128
+    CUtensorMap tm_x;   // bf16 [T][H], box 64 x 64
     CUtensorMap tm_w;   // bf16 [E][H], box 64 x E
     const uint16_t* g;  // bf16 [H] or nullptr
     int T, H, E, ld;
@@ -97,12 +98,13 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
                 *reinterpret_cast<uint4*>(sb + p.E * 128 + ((lane ^ (p.E & 7)) << 4)) = v;
                 fence_proxy_async_smem();
             }
+            __syncwarp();  // the gate row's writes, before lane 0's arrive releases the stage
+            if (lane == 0) mbar_arrive_expect_tx(full + s, kTileA + p.E * RK * 2);
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full + s, kTileA + p.E * RK * 2);
-                tma_load_2d(sa, &p.tm_x, kb * RK, t0, full + s);
-                tma_load_2d(sb, &p.tm_w, kb * RK, 0, full + s);
-            }
+            // the token tile as two 64-row boxes and the router rows, each from its own lane:
+            // copies issued by one thread are served one after another
+            if (lane < 2) tma_load_2d(sa + lane * (RM / 2) * 128, &p.tm_x, kb * RK, t0 + lane * (RM / 2), full + s);
+            if (lane == 2) tma_load_2d(sb, &p.tm_w, kb * RK, 0, full + s);
             issued = kb + 1;
         }
         if (*abort_flag && lane == 0) {
@@ -180,7 +182,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, cons
                                     float* logits, int* status, cudaStream_t st) {
     RouterTcArgs a{};
     if (!tmap_2d(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
-                 static_cast<uint64_t>(H) * 2, RK, RM, CU_TENSOR_MAP_SWIZZLE_128B))
+                 static_cast<uint64_t>(H) * 2, RK, RM / 2, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (!tmap_2d(&a.tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W_r, static_cast<uint64_t>(H), static_cast<uint64_t>(E),
                  static_cast<uint64_t>(H) * 2, RK, static_cast<uint32_t>(E), CU_TENSOR_MAP_SWIZZLE_128B))
