@@ -165,6 +165,102 @@ def dram_traffic(kernel, units):
     return None
 
 
+def time_layer(torch, layer, xs, steps, warmup, ids):
+    """CUDA-event time per layer call over `steps` calls cycling the inputs `xs`, and the mean
+    number of distinct experts those calls routed to."""
+    T, H = xs[0].shape
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+
+    def step(i):
+        layer.forward(xs[i % len(xs)], None, y=y, topk_ids_out=ids)
+
+    dt = time_loop(torch, step, steps, warmup)
+    nd = []
+    for i in range(len(xs)):
+        step(i)
+        nd.append(int(torch.unique(ids).numel()))
+    return 1e6 * dt / steps, float(np.mean(nd))
+
+
+def measure_glm(torch, moe, args):
+    """GLM-class decode layers (H=6144, I=2048, E=256, all experts resident: 5.4 GB, far above
+    L2), k=8 and k=32, T=1 and T=8, 8 distinct inputs cycled so that routing changes."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    hbm, _, _ = peaks()
+    H, I, E = 6144, 2048, 256
+    bpe = BYTES_PER_EXPERT(H, I)
+    out = {"workload": f"glm_class_decode_moe_layer H={H} I={I} E={E}", "bytes_per_expert": bpe}
+    base = upload(torch, moe, gen.Workload("g", 8, H, I, E, 8), 70)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    for k in (8, 32):
+        for T in (1, 8):
+            layer = moe.MoeLayer(base.W_r, base.experts, None, k, T)
+            xs = [to(gen.draw_x(1300 + i, T, H)) for i in range(8)]
+            ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+            us, nd = time_layer(torch, layer, xs, max(10, args.steps // 2), args.warmup, ids)
+            gbs = (nd * bpe + E * H * 2 + T * H * 8) / (us * 1e-6) / 1e9
+            out[f"k={k},T={T}"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6), "mean_distinct_experts": nd,
+                                   "hbm_gbs": gbs, "hbm_frac": gbs / hbm}
+    del base
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_router_sweep(torch, moe, args):
+    """Router + dispatch sweep: bf16 logits ~N(0,1)*2, k=8, E in {32..256}, T in {1..16384}; each
+    timed call (moe_router_topk then moe_dispatch) follows an untimed write of 256 MB, so L2
+    holds nothing of it.  Algorithmic bytes: T*E*2 + T*k*8 + T*k*12 + (E+1)*4."""
+    hbm, _, _ = peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    k, iters = 8, 20
+    out = {}
+    for E in (32, 64, 128, 256):
+        for T in (1, 64, 1024, 16384):
+            L = torch.from_numpy(gen.draw_logits(5, T, E).view(np.int16)).view(torch.bfloat16).cuda()
+            ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+            w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+            counts = torch.empty(E, dtype=torch.int32, device="cuda")
+            offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+            perm = torch.empty(T * k, dtype=torch.int32, device="cuda")
+            inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
+            ws = torch.zeros(moe.moe_dispatch_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            tot = 0.0
+            for i in range(iters + 3):
+                flush.fill_(i & 0xFF)
+                e0.record()
+                moe.moe_router_topk(L, E, k, ids, w)
+                moe.moe_dispatch(ids, E, counts, offsets, perm, inv, ws)
+                e1.record()
+                torch.cuda.synchronize()
+                if i >= 3:
+                    tot += e0.elapsed_time(e1) * 1e3
+            us = tot / iters
+            gbs = (T * E * 2 + T * k * 8 + T * k * 12 + (E + 1) * 4) / (us * 1e-6) / 1e9
+            out[f"E={E},T={T}"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm}
+    del flush
+    return out
+
+
+def measure_skewed_layer(torch, moe, args):
+    """Tiny-layer shape at T=8192 with Zipf(1.1)-skewed expert popularity (bias channel): both
+    roofs reported; the weights (8 experts, 0.4 MB) stay in L2 by nature."""
+    hbm, tc, _ = peaks()
+    wl = gen.WORKLOADS["tiny_zipf_t8192"]
+    inp = gen.draw_layer(wl)
+    W_r, Ed = upload_layer(torch, moe, inp)
+    layer = moe.MoeLayer(W_r, Ed, None, wl.k, wl.T)
+    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
+    ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
+    us, _ = time_layer(torch, layer, [x], max(10, args.steps // 2), args.warmup, ids)
+    flops = wl.T * (wl.k * 6 * wl.H * wl.I + 2 * wl.E * wl.H)
+    act_bytes = wl.T * wl.H * (2 + 4)
+    return {"workload": f"tiny_zipf_t8192 H={wl.H} I={wl.I} E={wl.E} k={wl.k} T={wl.T} (Zipf 1.1 popularity)",
+            "us_per_layer": us, "tokens_per_s": wl.T / (us * 1e-6),
+            "tflops": flops / (us * 1e-6) / 1e12, "tc_frac": flops / (us * 1e-6) / 1e12 / tc,
+            "act_gbs": act_bytes / (us * 1e-6) / 1e9, "act_hbm_frac": act_bytes / (us * 1e-6) / 1e9 / hbm}
+
+
 PREFILL = dict(name="qwen15_moe_a2.7b_prefill_layer", H=2048, I=1408, E=60, k=4, I_sh=5632, T=(4096, 512))
 
 
@@ -356,6 +452,11 @@ def run_ours(args, rank, world):
                             "graph_us": 1e6 * r["graph_s"] / max(10, args.steps // 2)}
 
     prefill = measure_prefill(torch, moe, args) if not args.no_prefill else None
+    extra = {}
+    if not args.no_extra:
+        extra = {"decode_glm": measure_glm(torch, moe, args),
+                 "router_dispatch_sweep": measure_router_sweep(torch, moe, args),
+                 "skewed_layer": measure_skewed_layer(torch, moe, args)}
     main["clocks"] = clocks.stop()
     if rank != 0:
         if dist is not None:
@@ -403,6 +504,7 @@ def run_ours(args, rank, world):
         "kernels_us_per_step": {n: 1e3 * v[0] / steps for n, v in kern.items()},
         "gpu_launches": int(round(main["launches_per_step"] * steps)),
         "prefill": prefill,
+        **extra,
         "clocks": main.get("clocks"),
         "e2e": {"value": world * T * steps / main["e2e_s"], "unit": "tokens/s",
                 "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
@@ -438,6 +540,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-layer section")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the GLM-class decode, router/dispatch sweep and skewed-layer sections")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
