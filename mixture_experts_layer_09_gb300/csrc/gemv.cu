@@ -170,8 +170,10 @@ struct Pipe {
     static constexpr int OFF_A = OFF_WS + NMAT * 32 * GRP * 2;
     static constexpr int OFF_AM = OFF_A + TB * KC * 2;
     static constexpr int OFF_HDR = OFF_AM + TB * GRP * 8;
-    static constexpr int STAGE = (OFF_HDR + 256 + 1023) / 1024 * 1024;
-    static constexpr int STAGES = (MODE == 0) ? 4 : 3;  // two CTAs fit one SM
+    // the boxes are unswizzled, so stage bases need 128-byte alignment only; four stages of
+    // either mode leave room for two CTAs per SM
+    static constexpr int STAGE = (OFF_HDR + 256 + 127) / 128 * 128;
+    static constexpr int STAGES = 4;
     static_assert(OFF_WS % 128 == 0 && OFF_A % 128 == 0 && OFF_AM % 16 == 0, "copy destinations aligned");
     static_assert(NMAT * NBOX <= kLaneScale && TB == 4, "one copy per producer lane; four tokens per pass");
 };
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
     using P = Pipe<MODE>;
     constexpr int NMAT = P::NMAT, S = P::STAGES, TB = P::TB;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * P::STAGE);
     uint64_t* empty = full + S;
     float* red = reinterpret_cast<float*>(empty + S);  // MODE 0: [TB][2][32]
@@ -759,7 +761,7 @@ bool gemv_tensor_maps(GemvArgs& p, int E) {
 template <int MODE>
 static size_t pipe_smem_bytes() {
     using P = Pipe<MODE>;
-    return 1024 + static_cast<size_t>(P::STAGES) * P::STAGE + 2 * P::STAGES * sizeof(uint64_t) +
+    return 128 + static_cast<size_t>(P::STAGES) * P::STAGE + 2 * P::STAGES * sizeof(uint64_t) +
            P::TB * 2 * 32 * sizeof(float) + 16;
 }
 
