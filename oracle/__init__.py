@@ -95,6 +95,21 @@ def router_topk(logits, k: int, E: Optional[int] = None):
     return ids, w
 
 
+def router_topk_v(logits, k: int, bias=None, renormalize: bool = True, scale: float = 1.0,
+                  E: Optional[int] = None):
+    """Router variants: selection over logits + bias, weights from the unbiased softmax,
+    renormalised over the picks or not, times scale."""
+    logits = _c(logits, np.float64)
+    T, ld = logits.shape
+    E = ld if E is None else E
+    b = None if bias is None else _c(bias, np.float64)
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float64)
+    _check(lib().mo_router_topk_v(_p(logits), ld, T, E, k, _p(b), 1 if renormalize else 0, C.c_double(scale),
+                                  _p(ids), _p(w)), "router_topk_v")
+    return ids, w
+
+
 def dispatch(ids, E: int):
     ids = _c(ids, np.int32)
     T, k = ids.shape

@@ -126,6 +126,52 @@ int mo_router_topk(const double* logits, int ld, int T, int E, int k,
     return rc;
 }
 
+/* Router variants: the definition written out step by step (see moe_oracle.h). */
+int mo_router_topk_v(const double* logits, int ld, int T, int E, int k, const double* bias,
+                     int renormalize, double scale, int32_t* ids, double* w) {
+    if (!logits || !ids || !w || T < 0 || E <= 0 || ld < E || k < 1 || k > E) return -1;
+    unsigned char* picked = (unsigned char*)malloc((size_t)E);
+    double* sc = (double*)malloc(sizeof(double) * (size_t)E);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    if (!picked || !sc || !p) { free(picked); free(sc); free(p); return -1; }
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; ++t) {
+        const double* l = logits + (size_t)t * ld;
+        for (int e = 0; e < E; ++e) {
+            sc[e] = l[e] + (bias ? bias[e] : 0.0);
+            if (!isfinite(l[e]) || !isfinite(sc[e])) rc = -2;
+        }
+        if (rc) break;
+        /* selection: k rounds of argmax over the biased scores, strict '>' */
+        memset(picked, 0, (size_t)E);
+        for (int round = 0; round < k; ++round) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (!picked[e] && (best < 0 || sc[e] > sc[best])) best = e;
+            picked[best] = 1;
+        }
+        /* weights: softmax of the unbiased logits over all E */
+        double m = l[0];
+        for (int e = 1; e < E; ++e)
+            if (l[e] > m) m = l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; ++e) z += exp(l[e] - m);
+        for (int e = 0; e < E; ++e) p[e] = exp(l[e] - m) / z;
+        double psel = 0.0;
+        for (int e = 0; e < E; ++e)
+            if (picked[e]) psel += p[e];
+        int q = 0;
+        for (int e = 0; e < E; ++e) {
+            if (!picked[e]) continue;
+            ids[(size_t)t * k + q] = e;
+            w[(size_t)t * k + q] = (renormalize ? p[e] / psel : p[e]) * scale;
+            ++q;
+        }
+    }
+    free(picked); free(sc); free(p);
+    return rc;
+}
+
 /* Bucket schedule (dasLLAMA #3988, routed-block commit: thread e counts expert
  * e's slots, exclusive scans place the buckets, the slot map lands in slot
  * order).  counts[e] = #{slots a : ids[a] == e}; offsets = exclusive scan with

@@ -50,6 +50,15 @@ int mo_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
 int mo_router_topk(const double* logits, int ld, int T, int E, int k,
                    int32_t* ids, double* w);
 
+/* Router variants (daScript PR #3988 "dasLLAMA vulkan: a MoE that fits the card ...", routed
+ * block commit, which names a router or selection bias and renormalised, scaled weights among
+ * the router shapes): selection over s_e = l_e + bias_e (bias NULL: 0), k rounds of argmax with
+ * the lowest index keeping a tie, picks in ascending expert id; weights from the unbiased
+ * logits: p = softmax(l) over all E, w_j = p[id_j] / sum over the picks of p when renormalize,
+ * else p[id_j]; then times scale.  bias = NULL, renormalize = 1, scale = 1 is mo_router_topk. */
+int mo_router_topk_v(const double* logits, int ld, int T, int E, int k, const double* bias,
+                     int renormalize, double scale, int32_t* ids, double* w);
+
 /* Per-expert histogram, exclusive scan and stable permutation of the T*k slots. */
 int mo_dispatch(const int32_t* ids, int T, int k, int E, int32_t* counts,
                 int32_t* offsets, int32_t* perm, int32_t* inv);

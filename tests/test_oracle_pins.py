@@ -332,3 +332,54 @@ def test_planted_mistakes_are_caught(oracle_lib):
     # renormalisation: top-2 of [0, 0, 0, 0] gives 1/2 each, not 1/4
     _, wt = oracle_lib.router_topk(np.zeros((1, 4)), 2)
     assert np.allclose(wt, 0.5)
+
+
+# ----------------------------------------------------------------------------- router variants
+def test_router_variants_closed_form(oracle_lib):
+    """logits ln(1..4): softmax = (1 2 3 4)/10; top-2 = experts 2, 3."""
+    import math
+    L = np.log(np.array([[1.0, 2.0, 3.0, 4.0]]))
+    ids, w = oracle_lib.router_topk_v(L, 2, renormalize=False)
+    assert ids.tolist() == [[2, 3]]
+    np.testing.assert_allclose(w, [[0.3, 0.4]], rtol=1e-14)
+    ids, w = oracle_lib.router_topk_v(L, 2, renormalize=True)
+    np.testing.assert_allclose(w, [[3 / 7, 4 / 7]], rtol=1e-14)
+    ids, w = oracle_lib.router_topk_v(L, 2, renormalize=True, scale=2.5)
+    np.testing.assert_allclose(w, [[7.5 / 7, 10 / 7]], rtol=1e-14)
+    ids, w = oracle_lib.router_topk_v(L, 2, renormalize=False, scale=2.5)
+    np.testing.assert_allclose(w, [[0.75, 1.0]], rtol=1e-14)
+    assert math.isclose(float(w.sum()), 1.75, rel_tol=1e-14)
+
+
+def test_router_variants_bias_moves_selection_only(oracle_lib):
+    L = np.array([[0.0, 0.0, 0.0, 1.0]])
+    bias = np.array([5.0, 0.0, 0.0, 0.0])
+    ids, w = oracle_lib.router_topk_v(L, 1, bias=bias, renormalize=False)
+    assert ids.tolist() == [[0]]
+    np.testing.assert_allclose(w, [[1.0 / (3.0 + np.e)]], rtol=1e-14)  # unbiased softmax of expert 0
+    ids, w = oracle_lib.router_topk_v(L, 1, bias=bias, renormalize=True)
+    np.testing.assert_allclose(w, [[1.0]], rtol=1e-14)
+    # a tie on the biased scores keeps the lower index
+    ids, _ = oracle_lib.router_topk_v(np.array([[1.0, 0.0]]), 1, bias=np.array([0.0, 1.0]))
+    assert ids.tolist() == [[0]]
+
+
+def test_router_variants_brute_force_selection(oracle_lib):
+    g = np.random.default_rng(11)
+    for _ in range(200):
+        E = int(g.integers(2, 9))
+        k = int(g.integers(1, E + 1))
+        L = g.choice([-1.0, 0.0, 0.5, 1.0], size=(1, E))
+        b = g.choice([0.0, 0.5, -0.5], size=E)
+        ids, _ = oracle_lib.router_topk_v(L, k, bias=b, renormalize=bool(g.integers(0, 2)))
+        s = L[0] + b
+        order = sorted(range(E), key=lambda e: (-s[e], e))[:k]
+        assert ids[0].tolist() == sorted(order)
+
+
+def test_router_variants_reduce_to_the_softmax_router(oracle_lib):
+    L = np.random.default_rng(12).normal(0, 2, size=(16, 60))
+    ids0, w0 = oracle_lib.router_topk(L, 4)
+    ids1, w1 = oracle_lib.router_topk_v(L, 4)
+    assert np.array_equal(ids0, ids1)
+    np.testing.assert_allclose(w1, w0, rtol=1e-15)
