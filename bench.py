@@ -238,6 +238,22 @@ def measure_router_sweep(torch, moe, args):
             us = tot / iters
             gbs = (T * E * 2 + T * k * 8 + T * k * 12 + (E + 1) * 4) / (us * 1e-6) / 1e9
             out[f"E={E},T={T}"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm}
+            if E == 256 and T == 16384:
+                # the router variant: selection bias, weights not renormalised, scaled
+                bias = torch.from_numpy(gen.rng(6, E).normal(0.0, 0.5, size=E).astype(np.float32)).cuda()
+                tot = 0.0
+                for i in range(iters + 3):
+                    flush.fill_(i & 0xFF)
+                    e0.record()
+                    moe.moe_router_topk_v(L, E, k, ids, w, sel_bias=bias, renormalize=False, scale=2.5)
+                    moe.moe_dispatch(ids, E, counts, offsets, perm, inv, ws)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    if i >= 3:
+                        tot += e0.elapsed_time(e1) * 1e3
+                us = tot / iters
+                gbs = (T * E * 2 + E * 4 + T * k * 8 + T * k * 12 + (E + 1) * 4) / (us * 1e-6) / 1e9
+                out[f"E={E},T={T},bias,unnormalised,scale=2.5"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm}
     del flush
     return out
 

@@ -132,6 +132,20 @@ MOE_API int moe_router_logits(const uint16_t* x, const uint16_t* W_r, const uint
 MOE_API int moe_router_topk(const void* logits, int logits_is_bf16, int ld, int T, int E,
                     int k, int32_t* topk_ids, float* topk_w, moe_stream_t stream);
 
+/* Router variants (daScript PR #3988, routed block commit: among the router shapes the pages
+ * name are a router or selection bias and renormalised, scaled weights).  The picks are the k
+ * largest of logits[t][e] + sel_bias[e] (lowest index on a tie, NaN never picked), written in
+ * ascending expert id; the weights come from the unbiased logits:
+ *   p = softmax(logits[t]) over all E;  topk_w = (renormalize ? p[id] / sum of p over the picks
+ *   : p[id]) * scale.
+ *   sel_bias  device fp32 [E], 4-byte aligned, or NULL (no bias)
+ *   scale     finite (else MOE_ERR_INVALID_ARG)
+ * Other arguments and limits as moe_router_topk; sel_bias = NULL, renormalize = 1, scale = 1
+ * is moe_router_topk. */
+MOE_API int moe_router_topk_v(const void* logits, int logits_is_bf16, int ld, int T, int E, int k,
+                              const float* sel_bias, int renormalize, float scale, int32_t* topk_ids,
+                              float* topk_w, moe_stream_t stream);
+
 /* Dispatch (stage 2): atomic-free per-expert histogram, exclusive scan and a
  * stable permutation of the T*k slots a = t*k + j.
  *   counts   int32 [E] or NULL     offsets int32 [E+1] (offsets[E] = T*k)

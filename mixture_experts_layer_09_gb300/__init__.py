@@ -58,6 +58,7 @@ _SIGS = {
     "moe_version": (C.c_char_p, []),
     "moe_router_logits": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_router_topk": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_router_topk_v": (_I, [_P, _I, _I, _I, _I, _I, _P, _I, C.c_float, _P, _P, _P]),
     "moe_dispatch_workspace_size": (_S, [_I, _I, _I]),
     "moe_dispatch": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
     "moe_dispatch_static": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -193,6 +194,23 @@ def moe_router_topk(logits, E: int, k: int, topk_ids, topk_w, stream=None):
     is_bf16 = 1 if logits.element_size() == 2 else 0
     _check(lib().moe_router_topk(_ptr(logits), is_bf16, ld, T, E, k, _ptr(topk_ids), _ptr(topk_w),
                                  _stream(stream)), "moe_router_topk")
+    return topk_ids, topk_w
+
+
+def moe_router_topk_v(logits, E: int, k: int, topk_ids, topk_w, sel_bias=None, renormalize: bool = True,
+                      scale: float = 1.0, stream=None):
+    """Router variants: selection over logits + sel_bias (fp32 [E] or None), weights from the
+    unbiased softmax, renormalised over the picks or not, times scale."""
+    T, ld = logits.shape
+    _need(logits, logits.element_size(), "logits")
+    _need(topk_ids, 4, "topk_ids")
+    _need(topk_w, 4, "topk_w")
+    if sel_bias is not None:
+        _need(sel_bias, 4, "sel_bias")
+    is_bf16 = 1 if logits.element_size() == 2 else 0
+    _check(lib().moe_router_topk_v(_ptr(logits), is_bf16, ld, T, E, k, _ptr(sel_bias), 1 if renormalize else 0,
+                                   float(scale), _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
+           "moe_router_topk_v")
     return topk_ids, topk_w
 
 

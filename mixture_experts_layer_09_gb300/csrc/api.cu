@@ -295,6 +295,18 @@ int moe_router_topk(const void* logits, int logits_is_bf16, int ld, int T, int E
     return status_of(launch_router_topk(logits, logits_is_bf16 != 0, ld, T, E, k, topk_ids, topk_w, S(stream)));
 }
 
+int moe_router_topk_v(const void* logits, int logits_is_bf16, int ld, int T, int E, int k, const float* sel_bias,
+                      int renormalize, float scale, int32_t* topk_ids, float* topk_w, moe_stream_t stream) {
+    if (T < 0 || E < 1 || E > MOE_MAX_E || k < 1 || k > E || k > MOE_MAX_K || ld < E) return MOE_ERR_INVALID_ARG;
+    if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (sel_bias && (reinterpret_cast<uintptr_t>(sel_bias) & 3u)) return MOE_ERR_INVALID_ARG;
+    if (int s = check_device()) return s;
+    return status_of(launch_router_topk(logits, logits_is_bf16 != 0, ld, T, E, k, topk_ids, topk_w, S(stream),
+                                        sel_bias, renormalize != 0, scale));
+}
+
 size_t moe_dispatch_workspace_size(int T, int k, int E) {
     if (T < 0 || k < 1 || E < 1) return 0;
     return kWsHead + align_up(sizeof(int32_t) * (E + 1), kWsAlign) +

@@ -37,8 +37,10 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, cons
                                     float* logits, int* status, cudaStream_t st);
 // group row stride of the quantised activations: K/32 rounded up to a multiple of 4
 inline int act_gld(int K) { return ((K / 32) + 3) & ~3; }
+// bias (fp32 [E], selection only), renorm, scale: the router variants (defaults: plain softmax top-k)
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
-                               float* w, cudaStream_t st);
+                               float* w, cudaStream_t st, const float* bias = nullptr, bool renorm = true,
+                               float scale = 1.f);
 
 // dispatch.cu
 // Decode batches (T <= 32): top-k of every token and the dispatch in one single-CTA launch.

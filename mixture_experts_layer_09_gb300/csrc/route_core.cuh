@@ -22,11 +22,15 @@ __device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p) { retur
 
 // VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
 // One warp selects the top-k of one logit row.  ids/w receive the row's k outputs.
+// Variants (bias, renorm, scale): the selection runs over logit + bias[e] (bias fp32 [E] or
+// null), the weights stay the unbiased softmax, renormalised over the picks or not, times scale.
 template <typename Tin, int VPT>
 __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E, int k, int32_t* __restrict__ ids,
-                                              float* __restrict__ w) {
+                                              float* __restrict__ w, const float* __restrict__ bias = nullptr,
+                                              bool renorm = true, float scale = 1.f) {
     const int lane = threadIdx.x & 31;
-    float v[VPT];
+    float v[VPT];   // logits: the softmax
+    float sv[VPT];  // selection scores: logit + bias
     bool picked[VPT];
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
@@ -34,9 +38,12 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
         if (e < E) {
             float f = load_logit<Tin>(row + e);
             v[j] = (f != f) ? -INFINITY : f;  // NaN never wins a pick
+            const float sb = bias ? v[j] + __ldg(bias + e) : v[j];
+            sv[j] = (sb != sb) ? -INFINITY : sb;
             picked[j] = false;
         } else {
             v[j] = -INFINITY;
+            sv[j] = -INFINITY;
             picked[j] = true;  // padding is never a candidate
         }
     }
@@ -47,8 +54,8 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int e = lane + 32 * j;
-            if (!picked[j] && (v[j] > bv || (v[j] == bv && e < bi))) {
-                bv = v[j];
+            if (!picked[j] && (sv[j] > bv || (sv[j] == bv && e < bi))) {
+                bv = sv[j];
                 bi = e;
             }
         }
@@ -100,7 +107,8 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
             if (pos < k) {
                 ids[pos] = lane + 32 * j;
                 // denominator guard: a row with no finite logit spreads the weight evenly
-                w[pos] = (psel > 0.f) ? p[j] / psel : 1.f / k;
+                const float wr = renorm ? ((psel > 0.f) ? p[j] / psel : 1.f / k) : p[j];
+                w[pos] = wr * scale;
             }
         }
         base += __popc(b);

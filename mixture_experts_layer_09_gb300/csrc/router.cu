@@ -196,24 +196,28 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const u
 template <typename Tin, int VPT>
 __global__ void __launch_bounds__(256) router_topk_warp_kernel(const Tin* __restrict__ logits, int ld, int T, int E,
                                                                int k, int32_t* __restrict__ topk_ids,
-                                                               float* __restrict__ topk_w) {
+                                                               float* __restrict__ topk_w,
+                                                               const float* __restrict__ bias, int renorm,
+                                                               float scale) {
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     topk_warp_row<Tin, VPT>(logits + static_cast<size_t>(t) * ld, E, k, topk_ids + static_cast<size_t>(t) * k,
-                            topk_w + static_cast<size_t>(t) * k);
+                            topk_w + static_cast<size_t>(t) * k, bias, renorm != 0, scale);
 }
 
 template <typename Tin>
 static cudaError_t launch_topk_t(const Tin* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
-                                 cudaStream_t st) {
+                                 const float* bias, bool renorm, float scale, cudaStream_t st) {
     const int vpt = (E + 31) / 32;
     const dim3 grid((T + 7) / 8), block(256);
     KernelScope ks_("router_topk", st);
     switch (vpt) {
 #define MOE_TOPK_CASE(V) \
-    case V: return launch_pdl(router_topk_warp_kernel<Tin, V>, grid, block, 0, st, logits, ld, T, E, k, ids, w);
+    case V:                                                                                                \
+        return launch_pdl(router_topk_warp_kernel<Tin, V>, grid, block, 0, st, logits, ld, T, E, k, ids, w, bias, \
+                          renorm ? 1 : 0, scale);
         MOE_TOPK_CASE(1)
         MOE_TOPK_CASE(2)
         MOE_TOPK_CASE(3)
@@ -228,10 +232,11 @@ static cudaError_t launch_topk_t(const Tin* logits, int ld, int T, int E, int k,
 }
 
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
-                               float* w, cudaStream_t st) {
+                               float* w, cudaStream_t st, const float* bias, bool renorm, float scale) {
     if (T == 0) return cudaSuccess;
-    if (is_bf16) return launch_topk_t(static_cast<const uint16_t*>(logits), ld, T, E, k, ids, w, st);
-    return launch_topk_t(static_cast<const float*>(logits), ld, T, E, k, ids, w, st);
+    if (is_bf16)
+        return launch_topk_t(static_cast<const uint16_t*>(logits), ld, T, E, k, ids, w, bias, renorm, scale, st);
+    return launch_topk_t(static_cast<const float*>(logits), ld, T, E, k, ids, w, bias, renorm, scale, st);
 }
 
 }  // namespace moe

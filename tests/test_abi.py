@@ -68,6 +68,13 @@ def test_host_argument_checks(L):
     assert L.moe_router_topk(fake, 0, 4, 4, 8, 2, fake, fake, None) == -1
     # T = 0 is a no-op
     assert L.moe_router_topk(None, 0, 8, 0, 8, 2, None, None, None) == 0
+    # router variants: a non-finite scale, a misaligned bias, k > E
+    f = C.c_float
+    assert L.moe_router_topk_v(fake, 0, 8, 4, 8, 2, None, 1, f(float("nan")), fake, fake, None) == -1
+    assert L.moe_router_topk_v(fake, 0, 8, 4, 8, 2, None, 1, f(float("inf")), fake, fake, None) == -1
+    assert L.moe_router_topk_v(fake, 0, 8, 4, 8, 2, C.c_void_p(0x1002), 1, f(1.0), fake, fake, None) == -1
+    assert L.moe_router_topk_v(fake, 0, 8, 4, 8, 9, None, 1, f(1.0), fake, fake, None) == -1
+    assert L.moe_router_topk_v(None, 0, 8, 0, 8, 2, None, 0, f(2.0), None, None, None) == 0
     # null pointers / misaligned pointers / H not a multiple of 32
     assert L.moe_router_logits(None, fake, None, 4, 256, 8, fake, None) == -1
     assert L.moe_router_logits(C.c_void_p(0x1002), fake, None, 4, 256, 8, fake, None) == -1

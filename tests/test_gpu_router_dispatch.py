@@ -42,6 +42,33 @@ def test_topk_sweep_bf16_logits(moe, E, T):
     assert np.allclose(w.sum(axis=1), 1.0, atol=1e-5)
 
 
+@pytest.mark.parametrize("E,k,bias,renorm,scale", [(60, 4, True, True, 1.0), (60, 4, True, False, 2.5),
+                                                    (256, 8, True, True, 2.5), (256, 8, False, False, 1.0),
+                                                    (128, 32, True, False, 1.0), (37, 5, False, True, 0.5)])
+def test_router_topk_variants(moe, E, k, bias, renorm, scale):
+    """Selection bias, no renormalisation, scaled weights against the oracle's definition; the
+    k-th margin is enforced on the biased scores, so no near-tie decides a pick."""
+    import torch
+    T = 333
+    g = gen.rng(7, E, k)
+    L = (g.normal(0.0, 2.0, size=(T, E))).astype(np.float32)
+    b = (g.normal(0.0, 0.5, size=E)).astype(np.float32) if bias else np.zeros(E, np.float32)
+    for t in range(T):
+        for a in range(64):
+            if wk.kth_margin(L[t].astype(np.float64) + b.astype(np.float64), k) >= wk.MARGIN:
+                break
+            L[t] = gen.rng(7, E, k, t, a).normal(0.0, 2.0, size=E).astype(np.float32)
+    ref_ids, ref_w = oracle.router_topk_v(L.astype(np.float64), k, bias=b.astype(np.float64) if bias else None,
+                                          renormalize=renorm, scale=scale)
+    ids = wk.poison(torch.empty((T, k), dtype=torch.int32, device="cuda"))
+    w = wk.poison(torch.empty((T, k), dtype=torch.float32, device="cuda"))
+    moe.moe_router_topk_v(wk.dev(L), E, k, ids, w, sel_bias=wk.dev(b) if bias else None, renormalize=renorm,
+                          scale=scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+    wk.assert_close(w.cpu().numpy(), ref_w, "topk_w (variant)")
+
+
 @pytest.mark.parametrize("E,k", [(8, 2), (60, 4), (256, 32), (37, 5), (256, 1), (16, 16)])
 def test_topk_ties_fp32(moe, E, k):
     """Tie-heavy rows (values from a set of 8): ties inside the picks and at the k-th boundary
