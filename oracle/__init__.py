@@ -110,6 +110,16 @@ def router_topk_v(logits, k: int, bias=None, renormalize: bool = True, scale: fl
     return ids, w
 
 
+def rmsnorm(y, gamma_bits, eps: float) -> np.ndarray:
+    """out[t] = y[t] / sqrt(mean(y[t]^2) + eps) * gamma (gamma as bf16 bits)."""
+    y = _c(y, np.float64)
+    T, H = y.shape
+    g = _c(gamma_bits, np.uint16)
+    out = np.empty((T, H), dtype=np.float64)
+    _check(lib().mo_rmsnorm(_p(y), _p(g), T, H, C.c_double(eps), _p(out)), "rmsnorm")
+    return out
+
+
 def dispatch(ids, E: int):
     ids = _c(ids, np.int32)
     T, k = ids.shape

@@ -350,3 +350,16 @@ done:
     free(perm); free(inv); free(rows); free(ysh);
     return rc;
 }
+
+/* RMSNorm (see moe_oracle.h): the mean of squares in fp64, one division per row. */
+int mo_rmsnorm(const double* y, const uint16_t* gamma, int T, int H, double eps, double* out) {
+    if (!y || !gamma || !out || T < 0 || H <= 0 || !(eps >= 0.0)) return -1;
+    for (int t = 0; t < T; ++t) {
+        const double* r = y + (size_t)t * H;
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) ss += r[h] * r[h];
+        const double inv = 1.0 / sqrt(ss / H + eps);
+        for (int h = 0; h < H; ++h) out[(size_t)t * H + h] = r[h] * inv * mo_bf16_to_f64(gamma[h]);
+    }
+    return 0;
+}

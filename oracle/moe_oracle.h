@@ -59,6 +59,12 @@ int mo_router_topk(const double* logits, int ld, int T, int E, int k,
 int mo_router_topk_v(const double* logits, int ld, int T, int E, int k, const double* bias,
                      int renormalize, double scale, int32_t* ids, double* w);
 
+/* RMSNorm of the layer output (daScript PR #3988, combine-folded residual commit: the add + RMS
+ * step after the routed block sums the FFN row onto the residual, then norms the row for the
+ * next layer):
+ * out[t][h] = y[t][h] / sqrt(mean_h y[t][h]^2 + eps) * gamma[h], gamma bf16 [H]. */
+int mo_rmsnorm(const double* y, const uint16_t* gamma, int T, int H, double eps, double* out);
+
 /* Per-expert histogram, exclusive scan and stable permutation of the T*k slots. */
 int mo_dispatch(const int32_t* ids, int T, int k, int E, int32_t* counts,
                 int32_t* offsets, int32_t* perm, int32_t* inv);

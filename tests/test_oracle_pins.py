@@ -383,3 +383,31 @@ def test_router_variants_reduce_to_the_softmax_router(oracle_lib):
     ids1, w1 = oracle_lib.router_topk_v(L, 4)
     assert np.array_equal(ids0, ids1)
     np.testing.assert_allclose(w1, w0, rtol=1e-15)
+
+
+# ----------------------------------------------------------------------------- RMSNorm after the combine
+def test_rmsnorm_closed_forms(oracle_lib):
+    one = gen.bf16_bits(np.ones(2, np.float32))
+    # y = (3, 4): mean of squares 12.5
+    out = oracle_lib.rmsnorm(np.array([[3.0, 4.0]]), one, 0.0)
+    np.testing.assert_allclose(out, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]], rtol=1e-15)
+    # gamma scales each column; eps enters under the root
+    g = gen.bf16_bits(np.array([2.0, 0.5], np.float32))
+    out = oracle_lib.rmsnorm(np.array([[3.0, 4.0]]), g, 0.5)
+    np.testing.assert_allclose(out, [[6 / math.sqrt(13.0), 2 / math.sqrt(13.0)]], rtol=1e-15)
+    # a zero row stays zero; a constant row c normalises to sign(c) when eps = 0
+    out = oracle_lib.rmsnorm(np.array([[0.0, 0.0], [-7.0, -7.0]]), one, 1e-6)
+    assert np.all(out[0] == 0.0)
+    np.testing.assert_allclose(out[1], [-7 / math.sqrt(49 + 1e-6)] * 2, rtol=1e-15)
+
+
+def test_rmsnorm_is_scale_invariant(oracle_lib):
+    y = np.random.default_rng(13).normal(0, 1, size=(5, 64))
+    g = gen.bf16_bits(np.random.default_rng(14).normal(1, 0.1, size=64).astype(np.float32))
+    a = oracle_lib.rmsnorm(y, g, 0.0)
+    b = oracle_lib.rmsnorm(37.5 * y, g, 0.0)
+    np.testing.assert_allclose(a, b, rtol=1e-13)
+    # unit root mean square before gamma
+    ones = gen.bf16_bits(np.ones(64, np.float32))
+    u = oracle_lib.rmsnorm(y, ones, 0.0)
+    np.testing.assert_allclose(np.sqrt(np.mean(u ** 2, axis=1)), 1.0, rtol=1e-13)
