@@ -182,6 +182,24 @@ def time_layer(torch, layer, xs, steps, warmup, ids):
     return 1e6 * dt / steps, float(np.mean(nd))
 
 
+def measure_norm(torch, moe, args, layers, T, H):
+    """The decode layer with its RMSNorm output (moe_layer_forward_norm) over the same cycled
+    replicas and inputs as the headline: us/layer with the extra pass."""
+    gamma = torch.from_numpy(gen.bf16_bits(gen.rng(23, H).normal(1.0, 0.1, size=H).astype(np.float32))
+                             .view(np.int16)).view(torch.bfloat16).cuda()
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    xs = [to(gen.draw_x(1500 + i, T, H)) for i in range(N_INPUTS)]
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    yn = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+
+    def step(i):
+        layers[i % len(layers)].forward(xs[i % N_INPUTS], None, y=y, norm_gamma=gamma, eps=1e-6, y_norm=yn)
+
+    steps = max(10, args.steps // 2)
+    dt = time_loop(torch, step, steps, args.warmup)
+    return {"us_per_layer_with_rmsnorm": 1e6 * dt / steps, "tokens_per_s": T * steps / dt}
+
+
 def measure_glm(torch, moe, args):
     """GLM-class decode layers (H=6144, I=2048, E=256, all experts resident: 5.4 GB, far above
     L2), k=8 and k=32, T=1 and T=8, 8 distinct inputs cycled so that routing changes."""
@@ -470,7 +488,8 @@ def run_ours(args, rank, world):
     prefill = measure_prefill(torch, moe, args) if not args.no_prefill else None
     extra = {}
     if not args.no_extra:
-        extra = {"decode_glm": measure_glm(torch, moe, args),
+        extra = {"decode_with_rmsnorm": measure_norm(torch, moe, args, layers, T, H),
+                 "decode_glm": measure_glm(torch, moe, args),
                  "router_dispatch_sweep": measure_router_sweep(torch, moe, args),
                  "skewed_layer": measure_skewed_layer(torch, moe, args)}
     main["clocks"] = clocks.stop()

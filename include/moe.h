@@ -210,6 +210,24 @@ MOE_API int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const
                       float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* RMSNorm of the layer output for the next layer (daScript PR #3988, combine-folded residual
+ * commit: after the routed block the residual row is normed for the next layer; the combine
+ * above already adds the residual, so this is the norm step):
+ *   y_norm[t][h] = bf16(y[t][h] / sqrt(mean_h y[t][h]^2 + eps) * gamma[h])
+ *   y fp32 [T][H] (16-byte aligned), gamma bf16 [H], y_norm bf16 [T][H] (both 8-byte aligned);
+ *   H a multiple of 32, eps >= 0 and finite (else MOE_ERR_INVALID_ARG).  The sum of squares is
+ *   fp32 in a fixed order; the output is rounded to nearest even. */
+MOE_API int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* y_norm,
+                        moe_stream_t stream);
+
+/* moe_layer_forward followed by moe_rmsnorm of its y (one more launch on the same stream):
+ * y receives the layer output, y_norm its RMSNorm with norm_gamma bf16 [H] and eps. */
+MOE_API int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r,
+                                   const moe_experts* W, const moe_shared* sh, int T, int k, float* y,
+                                   const uint16_t* norm_gamma, float eps, uint16_t* y_norm,
+                                   int32_t* topk_ids_out, float* topk_w_out, int arm, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
 /* Clears the head of a workspace (its first 4096 bytes: the device status word, the GEMV
  * arm's task claim counters and the down projection's column counters) on `stream`.  A
  * workspace must start with a zero head: call this once on a new workspace, or allocate it

@@ -68,6 +68,9 @@ _SIGS = {
     "moe_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "moe_layer_forward": (_I, [_P, _P, _P, C.POINTER(moe_experts), C.POINTER(moe_shared), _I, _I, _P, _P, _P,
                                _I, _P, _S, _P]),
+    "moe_rmsnorm": (_I, [_P, _P, _I, _I, C.c_float, _P, _P]),
+    "moe_layer_forward_norm": (_I, [_P, _P, _P, C.POINTER(moe_experts), C.POINTER(moe_shared), _I, _I, _P, _P,
+                                    C.c_float, _P, _P, _P, _I, _P, _S, _P]),
     "moe_workspace_init": (_I, [_P, _S, _P]),
     "moe_device_status": (_I, [_P, _S, C.POINTER(C.c_int), _P]),
     "moe_launch_count": (C.c_longlong, []),
@@ -283,6 +286,16 @@ def moe_layer_forward(x, residual, W_r, W: Experts, sh: Optional[Shared], k: int
     return y
 
 
+def moe_rmsnorm(y, gamma, eps: float, y_norm, stream=None):
+    """y_norm (bf16 [T][H]) = y / sqrt(mean(y^2) + eps) * gamma, per row of y (fp32 [T][H])."""
+    T, H = y.shape
+    _need(y, 4, "y")
+    _need(gamma, 2, "gamma")
+    _need(y_norm, 2, "y_norm")
+    _check(lib().moe_rmsnorm(_ptr(y), _ptr(gamma), T, H, float(eps), _ptr(y_norm), _stream(stream)), "moe_rmsnorm")
+    return y_norm
+
+
 def moe_workspace_init(ws, stream=None):
     _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
 
@@ -332,13 +345,21 @@ class MoeLayer:
         self._cs = shared.c() if shared is not None else None
 
     def forward(self, x, residual=None, y=None, topk_ids_out=None, topk_w_out=None, arm: int = ARM_AUTO,
-                stream=None):
+                stream=None, norm_gamma=None, eps: float = 1e-6, y_norm=None):
+        """y (fp32) = the layer; with norm_gamma and y_norm (bf16 [T][H]) also the RMSNorm of y."""
         import torch
         T = x.shape[0]
         if T > self.max_T:
             raise MoeError(-1, f"T={T} above this layer's workspace size (max_T={self.max_T})")
         if y is None:
             y = torch.empty((T, self.experts.H), dtype=torch.float32, device=x.device)
+        if norm_gamma is not None:
+            _check(lib().moe_layer_forward_norm(_ptr(x), _ptr(residual), _ptr(self.W_r), C.byref(self._cw),
+                                                C.byref(self._cs) if self._cs is not None else None, T, self.k,
+                                                _ptr(y), _ptr(norm_gamma), float(eps), _ptr(y_norm),
+                                                _ptr(topk_ids_out), _ptr(topk_w_out), arm, _ptr(self.ws),
+                                                self.ws.numel(), _stream(stream)), "moe_layer_forward_norm")
+            return y
         _check(lib().moe_layer_forward(_ptr(x), _ptr(residual), _ptr(self.W_r), C.byref(self._cw),
                                        C.byref(self._cs) if self._cs is not None else None, T, self.k, _ptr(y),
                                        _ptr(topk_ids_out), _ptr(topk_w_out), arm, _ptr(self.ws), self.ws.numel(),

@@ -460,6 +460,33 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     return run_gemm(mc, b, st);
 }
 
+int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* y_norm,
+                moe_stream_t stream) {
+    if (T < 0 || H < 32 || H > MOE_MAX_H || H % 32 || !(eps >= 0.f) || eps == INFINITY) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !gamma || !y_norm || !aligned16(y) || (reinterpret_cast<uintptr_t>(gamma) & 7u) ||
+        (reinterpret_cast<uintptr_t>(y_norm) & 7u))
+        return MOE_ERR_INVALID_ARG;
+    if (int s = check_device()) return s;
+    return status_of(launch_rmsnorm(y, gamma, T, H, eps, y_norm, S(stream)));
+}
+
+int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r, const moe_experts* W,
+                           const moe_shared* sh, int T, int k, float* y, const uint16_t* norm_gamma, float eps,
+                           uint16_t* y_norm, int32_t* topk_ids_out, float* topk_w_out, int arm, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+    if (int s = check_experts(W)) return s;
+    if (!(eps >= 0.f) || eps == INFINITY) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!norm_gamma || !y_norm || (reinterpret_cast<uintptr_t>(norm_gamma) & 7u) ||
+                  (reinterpret_cast<uintptr_t>(y_norm) & 7u)))
+        return MOE_ERR_INVALID_ARG;
+    if (int s = moe_layer_forward(x, residual, W_r, W, sh, T, k, y, topk_ids_out, topk_w_out, arm, ws, ws_bytes,
+                                  stream))
+        return s;
+    if (T == 0) return MOE_OK;
+    return status_of(launch_rmsnorm(y, norm_gamma, T, W->H, eps, y_norm, S(stream)));
+}
+
 int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (!ws || ws_bytes < kWsHead) return MOE_ERR_INVALID_ARG;
     return status_of(cudaMemsetAsync(ws, 0, kWsHead, S(stream)));

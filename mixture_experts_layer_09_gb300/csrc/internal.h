@@ -165,6 +165,11 @@ int gemm_ntile_max(int n_slots, int E);
 bool gemm_supported(int H, int I, int I_sh);
 cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st);
 
+// norm.cu: RMSNorm of the layer output into bf16 rows (H % 4 == 0, y 16-byte and gamma/out
+// 8-byte aligned)
+cudaError_t launch_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* out,
+                           cudaStream_t st);
+
 // combine.cu
 cudaError_t launch_combine(const float* rows, const int32_t* inv, const float* topk_w, bool weighted_slots,
                            const float* shared, const uint16_t* residual, int T, int k, int H, float* y,

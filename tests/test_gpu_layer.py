@@ -140,3 +140,53 @@ def test_layer_qwen15_prefill_gemv_arm_agrees(moe):
     inp = wk.layer("qwen15_prefill_t512", T=96)
     _check_layer(moe, inp, arm=1, sample=4)
     _check_layer(moe, inp, arm=2, sample=4)
+
+
+def _bf16_ulp_distance(a_bits, b_bits):
+    """Distance in bf16 steps between two arrays of bf16 bit patterns (monotone map of the
+    sign-magnitude encoding onto the integers)."""
+    def key(b):
+        b = b.astype(np.int64)
+        return np.where(b & 0x8000, 0x8000 - b, b)
+    return np.abs(key(a_bits) - key(b_bits))
+
+
+def _check_norm(y32, gamma_bits, eps, got_bits):
+    ref = oracle.rmsnorm(y32.astype(np.float64), gamma_bits, eps)
+    d = _bf16_ulp_distance(got_bits.view(np.uint16), gen.bf16_bits(ref.astype(np.float32)))
+    # the reference is rounded once from fp64 through fp32 to bf16; the kernel's fp32 path may
+    # land on the neighbouring bf16 value when the exact result sits at a rounding boundary
+    assert d.max() <= 1, f"max bf16 distance {d.max()}"
+    assert np.mean(d == 0) >= 0.99
+
+
+@pytest.mark.parametrize("T,H", [(37, 2048), (1, 256), (300, 6144)])
+def test_rmsnorm_stage(moe, T, H):
+    import torch
+    g = gen.rng(21, T, H)
+    y = (g.normal(0.0, 3.0, size=(T, H))).astype(np.float32)
+    gamma = gen.bf16_bits(g.normal(1.0, 0.1, size=H).astype(np.float32))
+    out = wk.poison(torch.empty((T, H), dtype=torch.int16, device="cuda"))
+    moe.moe_rmsnorm(wk.dev(y), wk.dev(gamma.view(np.int16), torch.bfloat16), 1e-6, out)
+    torch.cuda.synchronize()
+    _check_norm(y, gamma, 1e-6, out.cpu().numpy())
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_30b_decode_t16"])
+def test_layer_forward_norm(moe, name):
+    """The layer with its RMSNorm output: y identical to the plain layer call, y_norm the
+    oracle's RMSNorm of that y."""
+    import torch
+    inp = wk.layer(name)
+    x, r, W_r, E, S = wk.upload(inp)
+    wl = inp.wl
+    layer = moe.MoeLayer(W_r, E, S, wl.k, wl.T)
+    gamma = gen.bf16_bits(gen.rng(22, wl.H).normal(1.0, 0.1, size=wl.H).astype(np.float32))
+    gd = wk.dev(gamma.view(np.int16), torch.bfloat16)
+    y0 = layer.forward(x, r).clone()
+    y = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda"))
+    yn = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda"))
+    layer.forward(x, r, y=y, norm_gamma=gd, eps=1e-5, y_norm=yn)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0)
+    _check_norm(y.cpu().numpy(), gamma, 1e-5, yn.cpu().numpy())
