@@ -103,24 +103,27 @@ struct Item {
     int e, row0, nrows, mblk, K, M;
 };
 
-// Work item t: routed items first (tile-major, row blocks inner), then the shared expert's.
-// False when the item is past the tile schedule or has no rows (every role skips it alike).
+// Work item t: the shared expert's items first (the longest: full token tiles and, for down, the
+// longest K), then the routed ones (tile-major, row blocks inner), so that the last wave holds
+// short items.  False when the item is past the tile schedule or has no rows (every role skips
+// it alike).
 __device__ __forceinline__ bool item_at(const GemmK& p, int t, int n_tiles, Item& it) {
-    if (t < p.items_r) {
-        const int tix = t / p.mblk_r;
+    const int n_sh = p.items - p.items_r;
+    if (t >= n_sh) {
+        const int rt = t - n_sh;
+        const int tix = rt / p.mblk_r;
         if (tix >= n_tiles) return false;
         it.shared = false;
-        it.mblk = t % p.mblk_r;
+        it.mblk = rt % p.mblk_r;
         it.e = __ldg(p.tiles + 3 * tix);
         it.row0 = __ldg(p.tiles + 3 * tix + 1);
         it.nrows = __ldg(p.tiles + 3 * tix + 2);
         it.K = p.K_r;
         it.M = p.M_r;
     } else {
-        const int sid = t - p.items_r;
-        const int tix = sid / p.mblk_s;
+        const int tix = t / p.mblk_s;
         it.shared = true;
-        it.mblk = sid % p.mblk_s;
+        it.mblk = t % p.mblk_s;
         it.e = -1;
         it.row0 = tix * BN;
         it.nrows = min(BN, p.T - it.row0);
