@@ -15,6 +15,9 @@ Distributions follow the workloads the layer is measured on:
   even column in the low nibble; one fp16 scale per 32 K-columns drawn as
   |N(0, 0.01)| + 1e-3 (the grouped scales of colibri PR #418, "Grouped scales in
   the Vulkan kernels", at group size 32)
+* MXFP4 expert weights (the fmt=7 format of colibri PR #418's Kimi K3 tier): the same
+  uniform nibbles read as e2m1 codes, one ue8m0 exponent per 32 K-columns drawn uniform in
+  119..122 (scales 2^-8 .. 2^-5, weights of about the int4 sets' magnitude)
 * given router logits (router-only sweeps): bf16 of N(0, 1) * 2
 
 Every tensor draws from its own PCG64 stream keyed by (seed, tag, ...), and
@@ -60,11 +63,18 @@ def f16_to_f32(bits) -> np.ndarray:
 
 # ----------------------------------------------------------------------------- weights
 
+FMT_INT4, FMT_MXFP4 = "int4", "mxfp4"
+MXFP4_EXP_RANGE = (119, 122)  # ue8m0 exponents drawn uniform in this closed range
+
+
 @dataclass
 class Q4:
-    """One int4 matrix per expert: q [n_mat][rows][K/2] uint8, s [n_mat][rows][K/32] fp16 bits."""
+    """One 4-bit matrix per expert: q [n_mat][rows][K/2] uint8 (two codes per byte, the even
+    column in the low nibble) and s [n_mat][rows][K/32]: fp16 bits for int4, ue8m0 exponent
+    bytes for mxfp4."""
     q: np.ndarray
     s: np.ndarray
+    fmt: str = FMT_INT4
 
     @property
     def rows(self) -> int:
@@ -87,6 +97,28 @@ def draw_q4(seed: int, tag: int, n_mat: int, rows: int, K: int) -> Q4:
     return Q4(q, s)
 
 
+def draw_mxfp4(seed: int, tag: int, n_mat: int, rows: int, K: int) -> Q4:
+    """MXFP4 matrix: uniform e2m1 codes (the same stream as draw_q4's nibbles) and ue8m0
+    exponents uniform in MXFP4_EXP_RANGE."""
+    if K % SCALE_GROUP:
+        raise ValueError("K must be a multiple of 32")
+    g = rng(seed, tag)
+    nbytes = n_mat * rows * (K // 2)
+    raw = g.bit_generator.random_raw((nbytes + 7) // 8).view(np.uint8)
+    q = raw[:nbytes].reshape(n_mat, rows, K // 2).copy()
+    lo, hi = MXFP4_EXP_RANGE
+    e8 = g.integers(lo, hi + 1, size=(n_mat, rows, K // SCALE_GROUP), dtype=np.uint8)
+    return Q4(q, e8, FMT_MXFP4)
+
+
+def draw_mat(fmt: str, seed: int, tag: int, n_mat: int, rows: int, K: int) -> Q4:
+    if fmt == FMT_INT4:
+        return draw_q4(seed, tag, n_mat, rows, K)
+    if fmt == FMT_MXFP4:
+        return draw_mxfp4(seed, tag, n_mat, rows, K)
+    raise ValueError(f"unknown weight format {fmt!r}")
+
+
 @dataclass
 class Experts:
     E: int
@@ -95,6 +127,10 @@ class Experts:
     gate: Q4   # [E][I][H/2]
     up: Q4     # [E][I][H/2]
     down: Q4   # [E][H][I/2]
+
+    @property
+    def fmt(self) -> str:
+        return self.gate.fmt
 
 
 @dataclass
@@ -105,20 +141,24 @@ class Shared:
     down: Q4   # [1][H][I_sh/2]
     g: Optional[np.ndarray]  # bf16 bits [H], or None for an ungated shared expert
 
+    @property
+    def fmt(self) -> str:
+        return self.gate.fmt
 
-def draw_experts(seed: int, E: int, H: int, I: int) -> Experts:
+
+def draw_experts(seed: int, E: int, H: int, I: int, fmt: str = FMT_INT4) -> Experts:
     return Experts(E, H, I,
-                   draw_q4(seed, TAG_GATE, E, I, H),
-                   draw_q4(seed, TAG_UP, E, I, H),
-                   draw_q4(seed, TAG_DOWN, E, H, I))
+                   draw_mat(fmt, seed, TAG_GATE, E, I, H),
+                   draw_mat(fmt, seed, TAG_UP, E, I, H),
+                   draw_mat(fmt, seed, TAG_DOWN, E, H, I))
 
 
-def draw_shared(seed: int, H: int, I_sh: int, gated: bool = True) -> Shared:
+def draw_shared(seed: int, H: int, I_sh: int, gated: bool = True, fmt: str = FMT_INT4) -> Shared:
     g = bf16_bits(rng(seed, TAG_G).normal(0.0, 0.02, size=H)) if gated else None
     return Shared(I_sh,
-                  draw_q4(seed, TAG_SH_GATE, 1, I_sh, H),
-                  draw_q4(seed, TAG_SH_UP, 1, I_sh, H),
-                  draw_q4(seed, TAG_SH_DOWN, 1, H, I_sh),
+                  draw_mat(fmt, seed, TAG_SH_GATE, 1, I_sh, H),
+                  draw_mat(fmt, seed, TAG_SH_UP, 1, I_sh, H),
+                  draw_mat(fmt, seed, TAG_SH_DOWN, 1, H, I_sh),
                   g)
 
 
@@ -192,6 +232,8 @@ class Workload:
     gated_shared: bool = True
     residual: bool = True
     seed: int = 0
+    fmt: str = FMT_INT4     # routed experts' weight format
+    sh_fmt: str = FMT_INT4  # shared expert's weight format
     notes: str = ""
     extra: dict = field(default_factory=dict)
 
@@ -213,6 +255,11 @@ WORKLOADS = {
     "qwen15_prefill_t4096": Workload("qwen15_prefill_t4096", 4096, 2048, 1408, 60, 4, I_sh=5632),
     # tiny-layer shape at T=8192 with skewed (Zipf-like) expert popularity
     "tiny_zipf_t8192": Workload("tiny_zipf_t8192", 8192, 256, 128, 8, 2, zipf=1.1),
+    # MXFP4 routed experts (the int4 shared expert kept, as in colibri PR #418's Kimi K3 tier)
+    "qwen3_30b_decode_t16_mxfp4": Workload("qwen3_30b_decode_t16_mxfp4", 16, 2048, 768, 128, 8,
+                                           fmt=FMT_MXFP4),
+    "qwen15_prefill_t4096_mxfp4": Workload("qwen15_prefill_t4096_mxfp4", 4096, 2048, 1408, 60, 4,
+                                           I_sh=5632, fmt=FMT_MXFP4),
 }
 
 
@@ -228,8 +275,8 @@ class LayerInputs:
 
 def draw_layer(wl: Workload, x_attempts: Optional[dict] = None) -> LayerInputs:
     s = wl.seed
-    ex = draw_experts(s, wl.E, wl.H, wl.I)
-    sh = draw_shared(s, wl.H, wl.I_sh, wl.gated_shared) if wl.I_sh else None
+    ex = draw_experts(s, wl.E, wl.H, wl.I, wl.fmt)
+    sh = draw_shared(s, wl.H, wl.I_sh, wl.gated_shared, wl.sh_fmt) if wl.I_sh else None
     x = draw_x(s, wl.T, wl.H, x_attempts)
     W_r = draw_router(s, wl.E, wl.H)
     if wl.zipf > 0:

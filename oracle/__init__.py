@@ -42,6 +42,10 @@ def lib():
         _lib.mo_bf16_to_f64.argtypes = [C.c_uint16]
         _lib.mo_f16_to_f64.restype = C.c_double
         _lib.mo_f16_to_f64.argtypes = [C.c_uint16]
+        _lib.mo_e2m1_to_f64.restype = C.c_double
+        _lib.mo_e2m1_to_f64.argtypes = [C.c_int]
+        _lib.mo_ue8m0_to_f64.restype = C.c_double
+        _lib.mo_ue8m0_to_f64.argtypes = [C.c_uint8]
     return _lib
 
 
@@ -73,6 +77,26 @@ def dequant(q, s, rows: int, K: int) -> np.ndarray:
     q, s = _c(q, np.uint8), _c(s, np.uint16)
     w = np.empty((rows, K), dtype=np.float64)
     _check(lib().mo_dequant(_p(q), _p(s), rows, K, _p(w)), "dequant")
+    return w
+
+
+# weight formats (MO_FMT_INT4 / MO_FMT_MXFP4 of moe_oracle.h) and their scale element types
+FMT_CODES = {"int4": 0, "mxfp4": 1}
+SCALE_DTYPES = {"int4": np.uint16, "mxfp4": np.uint8}
+
+
+def e2m1_to_f64(nibble: int) -> float:
+    return lib().mo_e2m1_to_f64(int(nibble))
+
+
+def ue8m0_to_f64(e: int) -> float:
+    return lib().mo_ue8m0_to_f64(int(e))
+
+
+def dequant_mxfp4(q, e8, rows: int, K: int) -> np.ndarray:
+    q, e8 = _c(q, np.uint8), _c(e8, np.uint8)
+    w = np.empty((rows, K), dtype=np.float64)
+    _check(lib().mo_dequant_mxfp4(_p(q), _p(e8), rows, K, _p(w)), "dequant_mxfp4")
     return w
 
 
@@ -131,19 +155,22 @@ def dispatch(ids, E: int):
     return counts, offsets, perm, inv
 
 
-def expert_row(x_row, gate, up, down, H: int, I: int) -> np.ndarray:
-    """gate/up/down: (q, s) pairs of one expert."""
+def expert_row(x_row, gate, up, down, H: int, I: int, fmt: str = "int4") -> np.ndarray:
+    """gate/up/down: (q, s) pairs of one expert; s fp16 bits (int4) or ue8m0 bytes (mxfp4)."""
     x_row = _c(x_row, np.uint16)
-    arrs = [_c(gate[0], np.uint8), _c(gate[1], np.uint16), _c(up[0], np.uint8), _c(up[1], np.uint16),
-            _c(down[0], np.uint8), _c(down[1], np.uint16)]
+    sd = SCALE_DTYPES[fmt]
+    arrs = [_c(gate[0], np.uint8), _c(gate[1], sd), _c(up[0], np.uint8), _c(up[1], sd),
+            _c(down[0], np.uint8), _c(down[1], sd)]
     o = np.empty(H, dtype=np.float64)
-    _check(lib().mo_expert_row(_p(x_row), H, I, *[_p(a) for a in arrs], _p(o)), "expert_row")
+    _check(lib().mo_expert_row_fmt(_p(x_row), H, I, FMT_CODES[fmt], *[_p(a) for a in arrs], _p(o)),
+           "expert_row")
     return o
 
 
 def _exp_ptrs(ex):
-    arrs = [_c(ex.gate.q, np.uint8), _c(ex.gate.s, np.uint16), _c(ex.up.q, np.uint8),
-            _c(ex.up.s, np.uint16), _c(ex.down.q, np.uint8), _c(ex.down.s, np.uint16)]
+    sd = SCALE_DTYPES[ex.fmt]
+    arrs = [_c(ex.gate.q, np.uint8), _c(ex.gate.s, sd), _c(ex.up.q, np.uint8),
+            _c(ex.up.s, sd), _c(ex.down.q, np.uint8), _c(ex.down.s, sd)]
     return arrs
 
 
@@ -154,8 +181,8 @@ def expert_mlp(x, ex, ids, perm, token_mask=None) -> np.ndarray:
     arrs = _exp_ptrs(ex)
     tm = _c(token_mask, np.uint8)
     rows = np.zeros((T * k, H), dtype=np.float64)
-    _check(lib().mo_expert_mlp(_p(x), T, H, ex.I, ex.E, k, *[_p(a) for a in arrs],
-                               _p(ids), _p(perm), _p(tm), _p(rows)), "expert_mlp")
+    _check(lib().mo_expert_mlp_fmt(_p(x), T, H, ex.I, ex.E, k, FMT_CODES[ex.fmt], *[_p(a) for a in arrs],
+                                   _p(ids), _p(perm), _p(tm), _p(rows)), "expert_mlp")
     return rows
 
 
@@ -166,8 +193,8 @@ def shared_expert(x, sh, token_mask=None) -> np.ndarray:
     g = _c(sh.g, np.uint16)
     tm = _c(token_mask, np.uint8)
     y = np.zeros((T, H), dtype=np.float64)
-    _check(lib().mo_shared_expert(_p(x), T, H, sh.I_sh, *[_p(a) for a in arrs], _p(g), _p(tm), _p(y)),
-           "shared_expert")
+    _check(lib().mo_shared_expert_fmt(_p(x), T, H, sh.I_sh, FMT_CODES[sh.fmt], *[_p(a) for a in arrs], _p(g),
+                                      _p(tm), _p(y)), "shared_expert")
     return y
 
 
@@ -194,9 +221,9 @@ def layer_forward(inp, token_mask=None):
     if sh is not None:
         sarrs = _exp_ptrs(sh)
         sg = _c(sh.g, np.uint16)
-        I_sh = sh.I_sh
+        I_sh, fmt_s = sh.I_sh, FMT_CODES[sh.fmt]
     else:
-        sarrs, sg, I_sh = [None] * 6, None, 0
+        sarrs, sg, I_sh, fmt_s = [None] * 6, None, 0, 0
     tm = _c(token_mask, np.uint8)
     logits = np.empty((T, ex.E), dtype=np.float64)
     ids = np.empty((T, wl.k), dtype=np.int32)
@@ -204,7 +231,7 @@ def layer_forward(inp, token_mask=None):
     y = np.zeros((T, H), dtype=np.float64)
     r = _c(inp.residual, np.uint16)
     W_r = _c(inp.W_r, np.uint16)
-    _check(lib().mo_layer_forward(_p(x), _p(r), _p(W_r), T, H, ex.I, ex.E, wl.k,
-                                  *[_p(a) for a in arrs], I_sh, *[_p(a) for a in sarrs], _p(sg), _p(tm),
-                                  _p(logits), _p(ids), _p(w), _p(y)), "layer_forward")
+    _check(lib().mo_layer_forward_fmt(_p(x), _p(r), _p(W_r), T, H, ex.I, ex.E, wl.k, FMT_CODES[ex.fmt],
+                                      *[_p(a) for a in arrs], I_sh, fmt_s, *[_p(a) for a in sarrs], _p(sg),
+                                      _p(tm), _p(logits), _p(ids), _p(w), _p(y)), "layer_forward")
     return {"logits": logits, "ids": ids, "w": w, "y": y}

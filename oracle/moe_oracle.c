@@ -6,7 +6,8 @@
  * throughout, no blocking, fusion or reordering.  Single-threaded.
  *
  * Parity pins (tests/test_oracle_pins.py): brute-force full sort for top-k,
- * hand-decoded nibbles, closed forms of the MLP, dispatch invariants, the
+ * hand-decoded nibbles (int4 and MXFP4), closed forms of the MLP, the MXFP4 MLP against
+ * its exact int4 twin, dispatch invariants, the
  * zero-weight invariance of the combine, and tests/golden fixtures.
  */
 #include "moe_oracle.h"
@@ -54,6 +55,51 @@ int mo_dequant(const uint8_t* q, const uint16_t* s, int rows, int K, double* w) 
             w[(size_t)n * K + c] = weight_at(q, s, K, n, c);
     return 0;
 }
+
+/* e2m1 (OCP Microscaling formats, FP4 E2M1), decoded field by field: sign bit 3, exponent
+ * bits 2..1 with bias 1, mantissa bit 0; a zero exponent field is subnormal (m * 2^-1). */
+double mo_e2m1_to_f64(int nibble) {
+    int sign = (nibble >> 3) & 1;
+    int ex = (nibble >> 1) & 3;
+    int man = nibble & 1;
+    double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -v : v;
+}
+
+/* ue8m0 (OCP Microscaling formats, E8M0 scale): 2^(e - 127); e = 255 is NaN. */
+double mo_ue8m0_to_f64(uint8_t e) { return e == 255 ? NAN : ldexp(1.0, (int)e - 127); }
+
+/* One weight element of an MXFP4 matrix (colibri #418, fmt=7: an e2m1 nibble times the
+ * power-of-two scale of its 32-column group), in the int4 byte layout. */
+static double weight_at_mxfp4(const uint8_t* q, const uint8_t* e8, int K, int n, int c) {
+    uint8_t byte = q[(size_t)n * (K / 2) + c / 2];
+    int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
+    return mo_e2m1_to_f64(nib) * mo_ue8m0_to_f64(e8[(size_t)n * (K / 32) + c / 32]);
+}
+
+static int mxfp4_scales_finite(const uint8_t* e8, size_t n) {
+    for (size_t i = 0; i < n; ++i)
+        if (e8[i] == 255) return 0;
+    return 1;
+}
+
+int mo_dequant_mxfp4(const uint8_t* q, const uint8_t* e8, int rows, int K, double* w) {
+    if (!q || !e8 || !w || rows < 0 || K <= 0 || K % 32) return -1;
+    if (!mxfp4_scales_finite(e8, (size_t)rows * (K / 32))) return -2;
+    for (int n = 0; n < rows; ++n)
+        for (int c = 0; c < K; ++c)
+            w[(size_t)n * K + c] = weight_at_mxfp4(q, e8, K, n, c);
+    return 0;
+}
+
+/* Weight element (n, c) of a matrix in format fmt; s is fp16 scales or ue8m0 exponents. */
+static double weight_fmt(int fmt, const uint8_t* q, const void* s, int K, int n, int c) {
+    return fmt == MO_FMT_MXFP4 ? weight_at_mxfp4(q, (const uint8_t*)s, K, n, c)
+                               : weight_at(q, (const uint16_t*)s, K, n, c);
+}
+
+/* Bytes of one scale entry of format fmt. */
+static size_t scale_bytes(int fmt) { return fmt == MO_FMT_MXFP4 ? 1 : 2; }
 
 /* Router logits: one GEMV row per expert over the hidden row, and the shared
  * expert's gate logit as one more row "past the router's logits"
@@ -202,29 +248,69 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
 
 /* The fused expert group "gate+up+silu->down" (colibri #418, "Summary"):
  * g = W_g x, u = W_u x, h = silu(g) * u, o = W_d h. */
-int mo_expert_row(const uint16_t* x_row, int H, int I,
-                  const uint8_t* gq, const uint16_t* gs,
-                  const uint8_t* uq, const uint16_t* us,
-                  const uint8_t* dq, const uint16_t* ds, double* o) {
+int mo_expert_row_fmt(const uint16_t* x_row, int H, int I, int fmt,
+                      const uint8_t* gq, const void* gs,
+                      const uint8_t* uq, const void* us,
+                      const uint8_t* dq, const void* ds, double* o) {
     if (!x_row || !gq || !gs || !uq || !us || !dq || !ds || !o) return -1;
     if (H <= 0 || I <= 0 || H % 32 || I % 32) return -1;
+    if (fmt != MO_FMT_INT4 && fmt != MO_FMT_MXFP4) return -1;
+    if (fmt == MO_FMT_MXFP4 &&
+        (!mxfp4_scales_finite((const uint8_t*)gs, (size_t)I * (H / 32)) ||
+         !mxfp4_scales_finite((const uint8_t*)us, (size_t)I * (H / 32)) ||
+         !mxfp4_scales_finite((const uint8_t*)ds, (size_t)H * (I / 32))))
+        return -2;
     double* h = (double*)malloc(sizeof(double) * (size_t)I);
     if (!h) return -1;
     for (int i = 0; i < I; ++i) {
         double g = 0.0, u = 0.0;
         for (int c = 0; c < H; ++c) {
             double xv = mo_bf16_to_f64(x_row[c]);
-            g += weight_at(gq, gs, H, i, c) * xv;
-            u += weight_at(uq, us, H, i, c) * xv;
+            g += weight_fmt(fmt, gq, gs, H, i, c) * xv;
+            u += weight_fmt(fmt, uq, us, H, i, c) * xv;
         }
         h[i] = silu(g) * u;
     }
     for (int n = 0; n < H; ++n) {
         double acc = 0.0;
-        for (int i = 0; i < I; ++i) acc += weight_at(dq, ds, I, n, i) * h[i];
+        for (int i = 0; i < I; ++i) acc += weight_fmt(fmt, dq, ds, I, n, i) * h[i];
         o[n] = acc;
     }
     free(h);
+    return 0;
+}
+
+int mo_expert_row(const uint16_t* x_row, int H, int I,
+                  const uint8_t* gq, const uint16_t* gs,
+                  const uint8_t* uq, const uint16_t* us,
+                  const uint8_t* dq, const uint16_t* ds, double* o) {
+    return mo_expert_row_fmt(x_row, H, I, MO_FMT_INT4, gq, gs, uq, us, dq, ds, o);
+}
+
+int mo_expert_mlp_fmt(const uint16_t* x, int T, int H, int I, int E, int k, int fmt,
+                      const uint8_t* gate_q, const void* gate_s,
+                      const uint8_t* up_q, const void* up_s,
+                      const uint8_t* down_q, const void* down_s,
+                      const int32_t* ids, const int32_t* perm,
+                      const uint8_t* token_mask, double* rows) {
+    if (!x || !ids || !perm || !rows || T < 0 || E <= 0 || k < 1) return -1;
+    if (!gate_s || !up_s || !down_s) return -1;
+    size_t gq_sz = (size_t)I * (H / 2), gs_sz = (size_t)I * (H / 32) * scale_bytes(fmt);
+    size_t dq_sz = (size_t)H * (I / 2), ds_sz = (size_t)H * (I / 32) * scale_bytes(fmt);
+    const uint8_t* gs = (const uint8_t*)gate_s;  /* scale arrays walked in bytes */
+    const uint8_t* us = (const uint8_t*)up_s;
+    const uint8_t* ds = (const uint8_t*)down_s;
+    for (int r = 0; r < T * k; ++r) {
+        int a = perm[r], t = a / k, e = ids[a];
+        if (e < 0 || e >= E) return -1;
+        if (token_mask && !token_mask[t]) continue;
+        int rc = mo_expert_row_fmt(x + (size_t)t * H, H, I, fmt,
+                                   gate_q + e * gq_sz, gs + e * gs_sz,
+                                   up_q + e * gq_sz, us + e * gs_sz,
+                                   down_q + e * dq_sz, ds + e * ds_sz,
+                                   rows + (size_t)r * H);
+        if (rc) return rc;
+    }
     return 0;
 }
 
@@ -234,36 +320,23 @@ int mo_expert_mlp(const uint16_t* x, int T, int H, int I, int E, int k,
                   const uint8_t* down_q, const uint16_t* down_s,
                   const int32_t* ids, const int32_t* perm,
                   const uint8_t* token_mask, double* rows) {
-    if (!x || !ids || !perm || !rows || T < 0 || E <= 0 || k < 1) return -1;
-    size_t gq_sz = (size_t)I * (H / 2), gs_sz = (size_t)I * (H / 32);
-    size_t dq_sz = (size_t)H * (I / 2), ds_sz = (size_t)H * (I / 32);
-    for (int r = 0; r < T * k; ++r) {
-        int a = perm[r], t = a / k, e = ids[a];
-        if (e < 0 || e >= E) return -1;
-        if (token_mask && !token_mask[t]) continue;
-        int rc = mo_expert_row(x + (size_t)t * H, H, I,
-                               gate_q + e * gq_sz, gate_s + e * gs_sz,
-                               up_q + e * gq_sz, up_s + e * gs_sz,
-                               down_q + e * dq_sz, down_s + e * ds_sz,
-                               rows + (size_t)r * H);
-        if (rc) return rc;
-    }
-    return 0;
+    return mo_expert_mlp_fmt(x, T, H, I, E, k, MO_FMT_INT4, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                             ids, perm, token_mask, rows);
 }
 
 /* Shared expert scaled by sigmoid of its gate logit; an ungated shared expert
  * adds at weight one (dasLLAMA #3988, decode span commit). */
-int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,
-                     const uint8_t* gate_q, const uint16_t* gate_s,
-                     const uint8_t* up_q, const uint16_t* up_s,
-                     const uint8_t* down_q, const uint16_t* down_s,
-                     const uint16_t* g, const uint8_t* token_mask, double* y_sh) {
+int mo_shared_expert_fmt(const uint16_t* x, int T, int H, int I_sh, int fmt,
+                         const uint8_t* gate_q, const void* gate_s,
+                         const uint8_t* up_q, const void* up_s,
+                         const uint8_t* down_q, const void* down_s,
+                         const uint16_t* g, const uint8_t* token_mask, double* y_sh) {
     if (!x || !y_sh || T < 0) return -1;
     for (int t = 0; t < T; ++t) {
         if (token_mask && !token_mask[t]) continue;
         const uint16_t* xr = x + (size_t)t * H;
-        int rc = mo_expert_row(xr, H, I_sh, gate_q, gate_s, up_q, up_s, down_q, down_s,
-                               y_sh + (size_t)t * H);
+        int rc = mo_expert_row_fmt(xr, H, I_sh, fmt, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                                   y_sh + (size_t)t * H);
         if (rc) return rc;
         double gate = 1.0;
         if (g) {
@@ -274,6 +347,15 @@ int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,
         for (int n = 0; n < H; ++n) y_sh[(size_t)t * H + n] *= gate;
     }
     return 0;
+}
+
+int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,
+                     const uint8_t* gate_q, const uint16_t* gate_s,
+                     const uint8_t* up_q, const uint16_t* up_s,
+                     const uint8_t* down_q, const uint16_t* down_s,
+                     const uint16_t* g, const uint8_t* token_mask, double* y_sh) {
+    return mo_shared_expert_fmt(x, T, H, I_sh, MO_FMT_INT4, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                                g, token_mask, y_sh);
 }
 
 /* Combine onto the residual (dasLLAMA #3988: the routed slots weighted by the
@@ -299,17 +381,17 @@ int mo_combine(const double* rows, const int32_t* inv, const double* w,
     return 0;
 }
 
-int mo_layer_forward(const uint16_t* x, const uint16_t* residual,
-                     const uint16_t* W_r, int T, int H, int I, int E, int k,
-                     const uint8_t* gate_q, const uint16_t* gate_s,
-                     const uint8_t* up_q, const uint16_t* up_s,
-                     const uint8_t* down_q, const uint16_t* down_s,
-                     int I_sh,
-                     const uint8_t* sh_gate_q, const uint16_t* sh_gate_s,
-                     const uint8_t* sh_up_q, const uint16_t* sh_up_s,
-                     const uint8_t* sh_down_q, const uint16_t* sh_down_s,
-                     const uint16_t* sh_g, const uint8_t* token_mask,
-                     double* logits_out, int32_t* ids_out, double* w_out, double* y) {
+int mo_layer_forward_fmt(const uint16_t* x, const uint16_t* residual,
+                         const uint16_t* W_r, int T, int H, int I, int E, int k, int fmt_r,
+                         const uint8_t* gate_q, const void* gate_s,
+                         const uint8_t* up_q, const void* up_s,
+                         const uint8_t* down_q, const void* down_s,
+                         int I_sh, int fmt_s,
+                         const uint8_t* sh_gate_q, const void* sh_gate_s,
+                         const uint8_t* sh_up_q, const void* sh_up_s,
+                         const uint8_t* sh_down_q, const void* sh_down_s,
+                         const uint16_t* sh_g, const uint8_t* token_mask,
+                         double* logits_out, int32_t* ids_out, double* w_out, double* y) {
     if (!x || !W_r || !y || T < 0 || k < 1 || k > E) return -1;
     size_t nslot = (size_t)T * k;
     double* logits = (double*)malloc(sizeof(double) * ((size_t)T * E + 1));
@@ -333,12 +415,12 @@ int mo_layer_forward(const uint16_t* x, const uint16_t* residual,
     if (rc) goto done;
     rc = mo_dispatch(ids, T, k, E, counts, offsets, perm, inv);
     if (rc) goto done;
-    rc = mo_expert_mlp(x, T, H, I, E, k, gate_q, gate_s, up_q, up_s, down_q, down_s,
-                       ids, perm, token_mask, rows);
+    rc = mo_expert_mlp_fmt(x, T, H, I, E, k, fmt_r, gate_q, gate_s, up_q, up_s, down_q, down_s,
+                           ids, perm, token_mask, rows);
     if (rc) goto done;
     if (I_sh > 0) {
-        rc = mo_shared_expert(x, T, H, I_sh, sh_gate_q, sh_gate_s, sh_up_q, sh_up_s,
-                              sh_down_q, sh_down_s, sh_g, token_mask, ysh);
+        rc = mo_shared_expert_fmt(x, T, H, I_sh, fmt_s, sh_gate_q, sh_gate_s, sh_up_q, sh_up_s,
+                                  sh_down_q, sh_down_s, sh_g, token_mask, ysh);
         if (rc) goto done;
     }
     rc = mo_combine(rows, inv, w, ysh, residual, T, k, H, token_mask, y);
@@ -349,6 +431,22 @@ done:
     free(logits); free(ids); free(w); free(counts); free(offsets);
     free(perm); free(inv); free(rows); free(ysh);
     return rc;
+}
+
+int mo_layer_forward(const uint16_t* x, const uint16_t* residual,
+                     const uint16_t* W_r, int T, int H, int I, int E, int k,
+                     const uint8_t* gate_q, const uint16_t* gate_s,
+                     const uint8_t* up_q, const uint16_t* up_s,
+                     const uint8_t* down_q, const uint16_t* down_s,
+                     int I_sh,
+                     const uint8_t* sh_gate_q, const uint16_t* sh_gate_s,
+                     const uint8_t* sh_up_q, const uint16_t* sh_up_s,
+                     const uint8_t* sh_down_q, const uint16_t* sh_down_s,
+                     const uint16_t* sh_g, const uint8_t* token_mask,
+                     double* logits_out, int32_t* ids_out, double* w_out, double* y) {
+    return mo_layer_forward_fmt(x, residual, W_r, T, H, I, E, k, MO_FMT_INT4, gate_q, gate_s, up_q, up_s,
+                                down_q, down_s, I_sh, MO_FMT_INT4, sh_gate_q, sh_gate_s, sh_up_q, sh_up_s,
+                                sh_down_q, sh_down_s, sh_g, token_mask, logits_out, ids_out, w_out, y);
 }
 
 /* RMSNorm (see moe_oracle.h): the mean of squares in fp64, one division per row. */

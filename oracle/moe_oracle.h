@@ -38,6 +38,22 @@ double mo_f16_to_f64(uint16_t bits);
 /* Dequantise rows x K of one int4 matrix into w[rows][K] (fp64). */
 int mo_dequant(const uint8_t* q, const uint16_t* s, int rows, int K, double* w);
 
+/* MXFP4 weights (colibri PR #418, the fmt=7 note of its Kimi K3 Vulkan tier: e2m1 nibbles
+ * decoded through a table, one ue8m0 scale per 32 inputs).  The element and scale encodings are
+ * those of the OCP Microscaling (MX) formats: e2m1 has the sign in bit 3, a 2-bit exponent
+ * (bits 2..1, bias 1) and a 1-bit mantissa (bit 0), exponent field 0 meaning the subnormal
+ * value mantissa * 2^-1; ue8m0 is the power of two 2^(e - 127), e = 255 NaN.  Layout as for
+ * int4 (nibble (c & 1) of byte c/2, low first; the pages do not state the nibble order, the
+ * int4 layout's order is taken), exponents e8[row][K/32] one byte each. */
+double mo_e2m1_to_f64(int nibble);
+double mo_ue8m0_to_f64(uint8_t e);
+int mo_dequant_mxfp4(const uint8_t* q, const uint8_t* e8, int rows, int K, double* w);
+
+/* Weight formats of the _fmt functions below: the scale pointers are fp16 bits (uint16_t) for
+ * MO_FMT_INT4 and ue8m0 exponents (uint8_t) for MO_FMT_MXFP4. */
+#define MO_FMT_INT4 0
+#define MO_FMT_MXFP4 1
+
 /* logits[t][e] = sum_h x[t][h] * W_r[e][h] for e < E; when g != NULL also
  * logits[t][E] = sum_h x[t][h] * g[h] (the shared-expert gate row).  Row
  * stride of logits is E + (g != NULL). */
@@ -75,6 +91,10 @@ int mo_expert_row(const uint16_t* x_row, int H, int I,
                   const uint8_t* gq, const uint16_t* gs,
                   const uint8_t* uq, const uint16_t* us,
                   const uint8_t* dq, const uint16_t* ds, double* o);
+int mo_expert_row_fmt(const uint16_t* x_row, int H, int I, int fmt,
+                      const uint8_t* gq, const void* gs,
+                      const uint8_t* uq, const void* us,
+                      const uint8_t* dq, const void* ds, double* o);
 
 /* Expert outputs for every dispatched row r (dispatch order): a = perm[r],
  * t = a / k, e = ids[a]; rows[r][:] = expert e applied to x[t].  When
@@ -86,6 +106,12 @@ int mo_expert_mlp(const uint16_t* x, int T, int H, int I, int E, int k,
                   const uint8_t* down_q, const uint16_t* down_s,
                   const int32_t* ids, const int32_t* perm,
                   const uint8_t* token_mask, double* rows);
+int mo_expert_mlp_fmt(const uint16_t* x, int T, int H, int I, int E, int k, int fmt,
+                      const uint8_t* gate_q, const void* gate_s,
+                      const uint8_t* up_q, const void* up_s,
+                      const uint8_t* down_q, const void* down_s,
+                      const int32_t* ids, const int32_t* perm,
+                      const uint8_t* token_mask, double* rows);
 
 /* Shared expert: y_sh[t] = gate_t * W_d(silu(W_g x_t) * (W_u x_t)), where
  * gate_t = 1 / (1 + exp(-x_t . g)) when g != NULL and 1 otherwise. */
@@ -94,6 +120,11 @@ int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,
                      const uint8_t* up_q, const uint16_t* up_s,
                      const uint8_t* down_q, const uint16_t* down_s,
                      const uint16_t* g, const uint8_t* token_mask, double* y_sh);
+int mo_shared_expert_fmt(const uint16_t* x, int T, int H, int I_sh, int fmt,
+                         const uint8_t* gate_q, const void* gate_s,
+                         const uint8_t* up_q, const void* up_s,
+                         const uint8_t* down_q, const void* down_s,
+                         const uint16_t* g, const uint8_t* token_mask, double* y_sh);
 
 /* y[t][n] = residual[t][n] + shared[t][n] + sum_j w[t][j] * rows[inv[t*k+j]][n]
  * (residual bf16 and shared may be NULL). */
@@ -116,6 +147,18 @@ int mo_layer_forward(const uint16_t* x, const uint16_t* residual,
                      const uint8_t* sh_down_q, const uint16_t* sh_down_s,
                      const uint16_t* sh_g, const uint8_t* token_mask,
                      double* logits_f32, int32_t* ids, double* w, double* y);
+/* The same layer with the routed experts in format fmt_r and the shared expert in fmt_s. */
+int mo_layer_forward_fmt(const uint16_t* x, const uint16_t* residual,
+                         const uint16_t* W_r, int T, int H, int I, int E, int k, int fmt_r,
+                         const uint8_t* gate_q, const void* gate_s,
+                         const uint8_t* up_q, const void* up_s,
+                         const uint8_t* down_q, const void* down_s,
+                         int I_sh, int fmt_s,
+                         const uint8_t* sh_gate_q, const void* sh_gate_s,
+                         const uint8_t* sh_up_q, const void* sh_up_s,
+                         const uint8_t* sh_down_q, const void* sh_down_s,
+                         const uint16_t* sh_g, const uint8_t* token_mask,
+                         double* logits_f32, int32_t* ids, double* w, double* y);
 
 #ifdef __cplusplus
 }

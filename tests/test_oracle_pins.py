@@ -411,3 +411,126 @@ def test_rmsnorm_is_scale_invariant(oracle_lib):
     ones = gen.bf16_bits(np.ones(64, np.float32))
     u = oracle_lib.rmsnorm(y, ones, 0.0)
     np.testing.assert_allclose(np.sqrt(np.mean(u ** 2, axis=1)), 1.0, rtol=1e-13)
+
+
+# --------------------------------------------------------------------------- MXFP4 weights
+
+def test_e2m1_and_ue8m0_tables(oracle_lib):
+    # the element and scale value tables of the OCP MX specification, every code
+    d = _gold("mxfp4_decode.json")
+    for code, val in enumerate(d["e2m1_values"]):
+        got = oracle_lib.e2m1_to_f64(code)
+        assert got == val and math.copysign(1.0, got) == math.copysign(1.0, val), code
+    for e, val in d["ue8m0"].items():
+        assert oracle_lib.ue8m0_to_f64(int(e)) == val, e
+    assert math.isnan(oracle_lib.ue8m0_to_f64(255))
+
+
+def test_mxfp4_nibble_decode_golden(oracle_lib):
+    d = _gold("mxfp4_decode.json")
+    K = d["K"]
+    q = np.full((1, K // 2), int(d["default_byte"], 16), dtype=np.uint8)
+    for pos, b in d["bytes"].items():
+        q[0, int(pos)] = int(b, 16)
+    e8 = np.array([d["scales_e8"]], dtype=np.uint8)
+    w = oracle_lib.dequant_mxfp4(q, e8, 1, K)
+    for col, val in d["expected"].items():
+        got = w[0, int(col)]
+        assert got == val and math.copysign(1.0, got) == math.copysign(1.0, val), col
+    named = {int(c) for c in d["expected"]}
+    others = [c for c in range(K) if c not in named and c // 2 not in {int(p) for p in d["bytes"]}]
+    assert np.all(w[0, others] == 0.0)
+
+
+def test_mxfp4_nan_scale_is_rejected(oracle_lib):
+    q = np.zeros((1, 16), dtype=np.uint8)
+    e8 = np.array([[255]], dtype=np.uint8)
+    with pytest.raises(ValueError):
+        oracle_lib.dequant_mxfp4(q, e8, 1, 32)
+    x = gen.draw_x(3, 1, 32)
+    e8_ok = np.full((32, 1), 127, dtype=np.uint8)
+    with pytest.raises(ValueError):
+        oracle_lib.expert_row(x[0], (np.zeros((32, 16), np.uint8), e8_ok), (np.zeros((32, 16), np.uint8), e8_ok),
+                              (np.zeros((32, 16), np.uint8), np.full((32, 1), 255, np.uint8)), 32, 32, "mxfp4")
+
+
+def _int4_twin(q, e8):
+    """An int4 matrix holding the same weights as an MXFP4 matrix whose codes all have |2v| <= 7:
+    nibble 8 + 2v, fp16 scale 2^(e - 128) (exact in fp16 for the exponents used here)."""
+    two_v = {0: 0, 1: 1, 2: 2, 3: 3, 4: 4, 5: 6, 8: 0, 9: -1, 10: -2, 11: -3, 12: -4, 13: -6}
+    lo, hi = q & 0xF, q >> 4
+    lut = np.zeros(16, dtype=np.int64)
+    for c, v in two_v.items():
+        lut[c] = 8 + v
+    q4 = (lut[lo] | (lut[hi] << 4)).astype(np.uint8)
+    s = gen.f16_bits(np.ldexp(1.0, e8.astype(np.int64) - 128).astype(np.float32))
+    return q4, s
+
+
+def test_mxfp4_mlp_equals_its_int4_twin(oracle_lib):
+    # Codes 0..5 and 8..13 (values up to 3 in size) are int4 values 2v at half the scale, so
+    # both formats hold the same weights exactly and the two MLPs must agree to the last bit:
+    # a swapped nibble, a misplaced scale group or a transposed matrix on the MXFP4 side fails.
+    H, I = 64, 96
+    r = gen.rng(11, 1)
+    codes = np.array([0, 1, 2, 3, 4, 5, 8, 9, 10, 11, 12, 13], dtype=np.uint8)
+
+    def mat(rows, K):
+        lo = codes[r.integers(0, len(codes), size=(rows, K // 2))]
+        hi = codes[r.integers(0, len(codes), size=(rows, K // 2))]
+        return (lo | (hi << 4)).astype(np.uint8), r.integers(119, 123, size=(rows, K // 32)).astype(np.uint8)
+
+    g, u, d = mat(I, H), mat(I, H), mat(H, I)
+    x = gen.draw_x(5, 1, H)[0]
+    o_fp4 = oracle_lib.expert_row(x, g, u, d, H, I, "mxfp4")
+    o_int4 = oracle_lib.expert_row(x, _int4_twin(*g), _int4_twin(*u), _int4_twin(*d), H, I)
+    assert np.array_equal(o_fp4, o_int4)
+    # and the weights themselves
+    assert np.array_equal(oracle_lib.dequant_mxfp4(*g, I, H), oracle_lib.dequant(*_int4_twin(*g), I, H))
+
+
+def test_mxfp4_mlp_closed_form(oracle_lib):
+    # every gate and up weight +1.0 * 2^(e-127), every down weight -6 * 2^(e-127): with S = sum x,
+    # g = u = S * 2^(eg-127), h = silu(g) * u for every i, o[n] = -6 * 2^(ed-127) * I * h
+    H, I = 64, 32
+    x = gen.draw_x(7, 1, H)[0]
+    S = float(np.sum(gen.bf16_to_f32(x).astype(np.float64)))
+    one, m6 = 0x22, 0xFF  # both nibbles code 2 (+1.0); both nibbles code 15 (-6.0)
+    eg, ed = 126, 129
+    gq = np.full((I, H // 2), one, np.uint8)
+    ge = np.full((I, H // 32), eg, np.uint8)
+    dq = np.full((H, I // 2), m6, np.uint8)
+    de = np.full((H, I // 32), ed, np.uint8)
+    o = oracle_lib.expert_row(x, (gq, ge), (gq, ge), (dq, de), H, I, "mxfp4")
+    gv = S * 2.0 ** (eg - 127)
+    h = gv / (1.0 + math.exp(-gv)) * gv
+    ref = -6.0 * 2.0 ** (ed - 127) * I * h
+    assert np.allclose(o, ref, rtol=1e-12, atol=0)
+
+
+def test_mxfp4_layer_routes_like_int4(oracle_lib):
+    # the weight format changes the expert outputs, not the routing; with the routed experts in
+    # MXFP4 and the shared expert in int4 the layer is the sum of its parts
+    wl = gen.Workload("t", 3, 64, 32, 8, 2, I_sh=32, fmt=gen.FMT_MXFP4)
+    inp = gen.draw_layer(wl)
+    wl4 = gen.Workload("t", 3, 64, 32, 8, 2, I_sh=32)
+    inp4 = gen.draw_layer(wl4)
+    assert np.array_equal(inp.x, inp4.x) and inp.shared.fmt == "int4" and inp.experts.fmt == "mxfp4"
+    out = oracle_lib.layer_forward(inp)
+    out4 = oracle_lib.layer_forward(inp4)
+    assert np.array_equal(out["ids"], out4["ids"]) and np.array_equal(out["w"], out4["w"])
+    _, _, perm, inv = oracle_lib.dispatch(out["ids"], wl.E)
+    rows = oracle_lib.expert_mlp(inp.x, inp.experts, out["ids"], perm)
+    ysh = oracle_lib.shared_expert(inp.x, inp.shared)
+    y = oracle_lib.combine(rows, inv, out["w"], ysh, inp.residual)
+    assert np.allclose(out["y"], y, rtol=0, atol=1e-12)
+    assert not np.allclose(out["y"], out4["y"])
+
+
+def test_mxfp4_generator_ranges():
+    m = gen.draw_mxfp4(0, gen.TAG_GATE, 2, 32, 256)
+    assert m.fmt == "mxfp4" and m.s.dtype == np.uint8 and m.s.shape == (2, 32, 8)
+    lo, hi = gen.MXFP4_EXP_RANGE
+    assert m.s.min() >= lo and m.s.max() <= hi and len(np.unique(m.s)) == hi - lo + 1
+    # the codes are the int4 set's nibbles: same stream
+    assert np.array_equal(m.q, gen.draw_q4(0, gen.TAG_GATE, 2, 32, 256).q)
