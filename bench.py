@@ -136,10 +136,10 @@ def run_reference(args, rank):
 # hash taken over KERNEL_SOURCES by source_hash(); the GEMV kernels' unit is one distinct expert
 # streamed by the launch, so a launch's traffic is bytes_per_unit x its distinct experts.
 KERNEL_SOURCES = {
-    "gateup_gemv": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "internal.h"),
-    "down_gemv_combine": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "internal.h"),
-    "gemm_gateup": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "internal.h"),
-    "gemm_down": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "internal.h"),
+    "gateup_gemv": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
+    "down_gemv_combine": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
+    "gemm_gateup": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
+    "gemm_down": ("gemm_sm100.cu", "tcgen05.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
 }
 
 
@@ -295,6 +295,57 @@ def measure_skewed_layer(torch, moe, args):
             "act_gbs": act_bytes / (us * 1e-6) / 1e9, "act_hbm_frac": act_bytes / (us * 1e-6) / 1e9 / hbm}
 
 
+def measure_mxfp4(torch, moe, args):
+    """MXFP4 routed experts (e2m1 codes, expanded ue8m0 scales; the int4 shared expert kept):
+    the Qwen3-30B-A3B-shaped decode layer at T=16 (2 replicas of 340 MB cycled with 8 inputs)
+    and the Qwen1.5-MoE-A2.7B-shaped prefill layer at T=4096 (2 replicas of 300 MB)."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    hbm, tc, _ = peaks()
+    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    out = {}
+    H, I, E, k, T = 2048, 768, 128, 8, 16
+    layers = [upload(torch, moe, gen.Workload("m", T, H, I, E, k, fmt=gen.FMT_MXFP4), 80 + r) for r in range(2)]
+    xs = [to(gen.draw_x(1700 + i, T, H)) for i in range(8)]
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+
+    def step(i):
+        layers[i % 2].forward(xs[i % 8], None, y=y, topk_ids_out=ids)
+
+    steps = max(10, args.steps // 2)
+    dt = time_loop(torch, step, steps, args.warmup)
+    nd = []
+    for i in range(8):
+        step(i)
+        nd.append(int(torch.unique(ids).numel()))
+    us = 1e6 * dt / steps
+    gbs = (np.mean(nd) * BYTES_PER_EXPERT(H, I) + E * H * 2 + T * H * 8) / (us * 1e-6) / 1e9
+    out["qwen3_30b_decode_t16_mxfp4"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+                                         "mean_distinct_experts": float(np.mean(nd)), "hbm_gbs": gbs,
+                                         "hbm_frac": gbs / hbm}
+    del layers
+    P = PREFILL
+    T = 4096
+    layers = [upload(torch, moe, gen.Workload("mp", T, P["H"], P["I"], P["E"], P["k"], I_sh=P["I_sh"],
+                                              fmt=gen.FMT_MXFP4), 90 + r) for r in range(2)]
+    xs = [to(gen.draw_x(1900 + i, T, P["H"])) for i in range(4)]
+    y = torch.empty((T, P["H"]), dtype=torch.float32, device="cuda")
+
+    def pstep(i):
+        layers[i % 2].forward(xs[i % 4], None, y=y)
+
+    dt = time_loop(torch, pstep, steps, args.warmup)
+    us = 1e6 * dt / steps
+    Hh, Ii, kk, Ish = P["H"], P["I"], P["k"], P["I_sh"]
+    flops = 2.0 * T * (kk * 3 * Hh * Ii + 3 * Hh * Ish + Hh * (P["E"] + 1))
+    out["qwen15_prefill_t4096_mxfp4"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+                                         "layer_tflops": flops / (us * 1e-6) / 1e12,
+                                         "layer_tc_frac": flops / (us * 1e-6) / 1e12 / tc}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
 PREFILL = dict(name="qwen15_moe_a2.7b_prefill_layer", H=2048, I=1408, E=60, k=4, I_sh=5632, T=(4096, 512))
 
 
@@ -347,7 +398,7 @@ def upload_layer(torch, moe, inp):
         return (t.view(dtype) if dtype is not None else t).cuda()
 
     def q4(m):
-        return moe.Q4(dev(m.q), dev(m.s.view(np.int16), torch.float16))
+        return moe.upload_q4(m.q, m.s, m.fmt)
 
     ex = inp.experts
     E = moe.Experts(ex.E, ex.H, ex.I, q4(ex.gate), q4(ex.up), q4(ex.down))
@@ -491,7 +542,8 @@ def run_ours(args, rank, world):
         extra = {"decode_with_rmsnorm": measure_norm(torch, moe, args, layers, T, H),
                  "decode_glm": measure_glm(torch, moe, args),
                  "router_dispatch_sweep": measure_router_sweep(torch, moe, args),
-                 "skewed_layer": measure_skewed_layer(torch, moe, args)}
+                 "skewed_layer": measure_skewed_layer(torch, moe, args),
+                 "mxfp4": measure_mxfp4(torch, moe, args)}
     main["clocks"] = clocks.stop()
     if rank != 0:
         if dist is not None:

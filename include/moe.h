@@ -46,6 +46,13 @@
  *   moe_q4.s  fp16   [n_mat][rows][K/32]: scale of columns 32g .. 32g+31
  *   routed experts (n_mat = E): gate, up: rows = I, K = H; down: rows = H, K = I
  *   shared expert  (n_mat = 1): gate, up: rows = I_sh, K = H; down: rows = H, K = I_sh
+ * MXFP4 weights (fmt = MOE_WFMT_MXFP4; colibri #418, the fmt=7 note of its Kimi K3 tier: e2m1
+ * codes through a table, one ue8m0 scale per 32 inputs, the exponents expanded at upload):
+ *   moe_q4.q  the same layout; each nibble is an e2m1 code (OCP Microscaling formats: sign bit
+ *             3, exponent bits 2..1 with bias 1, mantissa bit 0), uploaded as stored
+ *   moe_q4.s  fp16 [n_mat][rows][K/32] = 2^(e - 128) for the group's ue8m0 exponent e, as
+ *             written by moe_mxfp4_scales(): half the MX scale, because the kernels read an
+ *             e2m1 code as the integer 2v (v the code's value), exactly
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -71,7 +78,13 @@ enum {
     MOE_ERR_UNSUPPORTED = -2,     /* valid request this build does not serve */
     MOE_ERR_CUDA = -3,            /* a CUDA call or launch failed (no device, bad stream, ...) */
     MOE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait ran out (recorded on device) */
-    MOE_ERR_DEVICE_INDEX = -5     /* a routed expert id outside [0, E) (recorded on device) */
+    MOE_ERR_DEVICE_INDEX = -5,    /* a routed expert id outside [0, E) (recorded on device) */
+    MOE_ERR_DEVICE_RANGE = -6     /* an MXFP4 scale exponent outside [104, 140] (recorded on device) */
+};
+
+enum {
+    MOE_WFMT_INT4 = 0,   /* offset-binary int4 (nibble - 8), fp16 scale per 32 columns */
+    MOE_WFMT_MXFP4 = 1   /* e2m1 codes, expanded ue8m0 scale per 32 columns (moe_mxfp4_scales) */
 };
 
 enum {
@@ -94,13 +107,25 @@ typedef struct {
 typedef struct {
     int E, H, I;        /* 1 <= E <= 256; H, I positive multiples of 32; H <= 24576 */
     moe_q4 gate, up, down;
+    int fmt;            /* MOE_WFMT_INT4 (0) or MOE_WFMT_MXFP4 (1), all three matrices alike */
 } moe_experts;
 
 typedef struct {
     int I_sh;           /* positive multiple of 32 */
     moe_q4 gate, up, down;
     const uint16_t* g;  /* device, bf16 [H] gate vector; NULL = ungated (weight 1) */
+    int fmt;            /* MOE_WFMT_*, independent of the routed experts' format */
 } moe_shared;
+
+/* Upload step of MXFP4 weights: expands n ue8m0 exponents e8 (device, uint8) into the fp16
+ * scales the kernels read, s[i] = 2^(e8[i] - 128) (device, fp16 [n], 2-byte aligned; written
+ * for every i).  Exponents in [104, 140] give exact products with every e2m1 code in fp16;
+ * an exponent outside that range (255, the MX NaN, included) writes 0 and records
+ * MOE_ERR_DEVICE_RANGE in the status word of the workspace ws (at least 4096 bytes, from
+ * moe_workspace_init or zeroed), which moe_device_status() reads.  Asynchronous on stream.
+ * Returns MOE_ERR_INVALID_ARG for null pointers or a short workspace. */
+MOE_API int moe_mxfp4_scales(const uint8_t* e8, size_t n, uint16_t* s, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
 
 /* Text of a status code (static storage). */
 MOE_API const char* moe_status_string(int status);

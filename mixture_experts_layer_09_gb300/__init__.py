@@ -45,11 +45,16 @@ class moe_q4(C.Structure):
 
 class moe_experts(C.Structure):
     _fields_ = [("E", C.c_int), ("H", C.c_int), ("I", C.c_int),
-                ("gate", moe_q4), ("up", moe_q4), ("down", moe_q4)]
+                ("gate", moe_q4), ("up", moe_q4), ("down", moe_q4), ("fmt", C.c_int)]
 
 
 class moe_shared(C.Structure):
-    _fields_ = [("I_sh", C.c_int), ("gate", moe_q4), ("up", moe_q4), ("down", moe_q4), ("g", C.c_void_p)]
+    _fields_ = [("I_sh", C.c_int), ("gate", moe_q4), ("up", moe_q4), ("down", moe_q4), ("g", C.c_void_p),
+                ("fmt", C.c_int)]
+
+
+# weight formats (MOE_WFMT_*)
+WFMT = {"int4": 0, "mxfp4": 1}
 
 
 _P, _I, _S = C.c_void_p, C.c_int, C.c_size_t
@@ -72,6 +77,7 @@ _SIGS = {
     "moe_layer_forward_norm": (_I, [_P, _P, _P, C.POINTER(moe_experts), C.POINTER(moe_shared), _I, _I, _P, _P,
                                     C.c_float, _P, _P, _P, _I, _P, _S, _P]),
     "moe_workspace_init": (_I, [_P, _S, _P]),
+    "moe_mxfp4_scales": (_I, [_P, _S, _P, _P, _S, _P]),
     "moe_device_status": (_I, [_P, _S, C.POINTER(C.c_int), _P]),
     "moe_launch_count": (C.c_longlong, []),
     "moe_profile_enable": (_I, [_I]),
@@ -132,14 +138,24 @@ def _need(t, dtype_size: int, what: str):
 
 @dataclass
 class Q4:
-    """One int4 matrix stack on the device: q uint8 [n][rows][K/2], s fp16 [n][rows][K/32]."""
+    """One 4-bit matrix stack on the device: q uint8 [n][rows][K/2], s fp16 [n][rows][K/32].
+    fmt "int4": offset-binary nibbles and their scales; "mxfp4": e2m1 codes and the scales
+    moe_mxfp4_scales() expanded from the ue8m0 exponents (see upload_q4)."""
     q: "torch.Tensor"
     s: "torch.Tensor"
+    fmt: str = "int4"
 
     def c(self) -> moe_q4:
         _need(self.q, 1, "q")
         _need(self.s, 2, "s")
         return moe_q4(self.q.data_ptr(), self.s.data_ptr())
+
+
+def _fmt_of(*mats: Q4) -> int:
+    fmts = {m.fmt for m in mats}
+    if len(fmts) != 1 or next(iter(fmts)) not in WFMT:
+        raise MoeError(-1, f"gate, up and down must share one known weight format, got {sorted(fmts)}")
+    return WFMT[fmts.pop()]
 
 
 @dataclass
@@ -152,7 +168,8 @@ class Experts:
     down: Q4
 
     def c(self) -> moe_experts:
-        return moe_experts(self.E, self.H, self.I, self.gate.c(), self.up.c(), self.down.c())
+        return moe_experts(self.E, self.H, self.I, self.gate.c(), self.up.c(), self.down.c(),
+                           _fmt_of(self.gate, self.up, self.down))
 
 
 @dataclass
@@ -165,7 +182,8 @@ class Shared:
 
     def c(self) -> moe_shared:
         _need(self.g, 2, "g")
-        return moe_shared(self.I_sh, self.gate.c(), self.up.c(), self.down.c(), _ptr(self.g))
+        return moe_shared(self.I_sh, self.gate.c(), self.up.c(), self.down.c(), _ptr(self.g),
+                          _fmt_of(self.gate, self.up, self.down))
 
 
 def _workspace(nbytes: int, device):
@@ -177,6 +195,40 @@ def _workspace(nbytes: int, device):
 
 def moe_version() -> str:
     return lib().moe_version().decode()
+
+
+def moe_mxfp4_scales(e8, s, ws, stream=None):
+    """Expands ue8m0 exponents e8 (uint8, device) into the fp16 scales s = 2^(e - 128) the
+    kernels read; an exponent outside [104, 140] is recorded in ws's status word."""
+    _need(e8, 1, "e8")
+    _need(s, 2, "s")
+    if e8.numel() != s.numel():
+        raise MoeError(-1, "e8 and s must have the same number of elements")
+    _check(lib().moe_mxfp4_scales(_ptr(e8), e8.numel(), _ptr(s), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _stream(stream)), "moe_mxfp4_scales")
+    return s
+
+
+def upload_q4(q, s, fmt: str = "int4", device="cuda") -> Q4:
+    """Device copy of one host matrix stack (numpy): q uint8 codes; s fp16 bits (int4) or
+    ue8m0 exponent bytes (mxfp4, expanded on the device by moe_mxfp4_scales).  Synchronises
+    and raises when an exponent is out of range."""
+    import numpy as np
+    import torch
+    qd = torch.from_numpy(np.ascontiguousarray(q, dtype=np.uint8)).to(device)
+    if fmt == "int4":
+        sd = torch.from_numpy(np.ascontiguousarray(s, dtype=np.uint16).view(np.int16)).to(device).view(torch.float16)
+        return Q4(qd, sd, "int4")
+    if fmt != "mxfp4":
+        raise MoeError(-1, f"unknown weight format {fmt!r}")
+    e8 = torch.from_numpy(np.ascontiguousarray(s, dtype=np.uint8)).to(device)
+    sd = torch.empty(e8.shape, dtype=torch.float16, device=device)
+    ws = _workspace(4096, device)
+    moe_mxfp4_scales(e8, sd, ws)
+    st = moe_device_status(ws)
+    if st != 0:
+        raise MoeError(st, "moe_mxfp4_scales: scale exponent outside [104, 140]")
+    return Q4(qd, sd, "mxfp4")
 
 
 def moe_router_logits(x, W_r, g, logits, stream=None):

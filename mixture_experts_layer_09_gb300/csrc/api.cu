@@ -118,6 +118,7 @@ int check_experts(const moe_experts* W) {
     if (!W) return MOE_ERR_INVALID_ARG;
     if (W->E < 1 || W->E > MOE_MAX_E || W->H < 32 || W->I < 32 || W->H % 32 || W->I % 32) return MOE_ERR_INVALID_ARG;
     if (W->H > MOE_MAX_H) return MOE_ERR_INVALID_ARG;
+    if (W->fmt != MOE_WFMT_INT4 && W->fmt != MOE_WFMT_MXFP4) return MOE_ERR_INVALID_ARG;
     int s;
     if ((s = check_q4(W->gate)) || (s = check_q4(W->up)) || (s = check_q4(W->down))) return s;
     return MOE_OK;
@@ -126,6 +127,7 @@ int check_experts(const moe_experts* W) {
 int check_shared(const moe_shared* sh) {
     if (!sh) return MOE_OK;
     if (sh->I_sh < 32 || sh->I_sh % 32) return MOE_ERR_INVALID_ARG;
+    if (sh->fmt != MOE_WFMT_INT4 && sh->fmt != MOE_WFMT_MXFP4) return MOE_ERR_INVALID_ARG;
     int s;
     if ((s = check_q4(sh->gate)) || (s = check_q4(sh->up)) || (s = check_q4(sh->down))) return s;
     if (sh->g && !aligned16(sh->g)) return MOE_ERR_INVALID_ARG;
@@ -200,6 +202,8 @@ int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
     p.max_active = std::min(W->E, c.T * c.k);
     p.gate_q = W->gate.q; p.gate_s = W->gate.s; p.up_q = W->up.q; p.up_s = W->up.s;
     p.down_q = W->down.q; p.down_s = W->down.s;
+    p.fp4_r = W->fmt == MOE_WFMT_MXFP4;
+    p.fp4_s = c.sh && c.sh->fmt == MOE_WFMT_MXFP4;
     p.sh_I = I_sh;
     if (c.sh) {
         p.sh_gate_q = c.sh->gate.q; p.sh_gate_s = c.sh->gate.s; p.sh_up_q = c.sh->up.q; p.sh_up_s = c.sh->up.s;
@@ -240,6 +244,8 @@ int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st) {
     p.logit_ld = c.logit_ld;
     p.gate_q = W->gate.q; p.gate_s = W->gate.s; p.up_q = W->up.q; p.up_s = W->up.s;
     p.down_q = W->down.q; p.down_s = W->down.s;
+    p.fp4_r = W->fmt == MOE_WFMT_MXFP4;
+    p.fp4_s = c.sh && c.sh->fmt == MOE_WFMT_MXFP4;
     if (c.sh) {
         p.sh_gate_q = c.sh->gate.q; p.sh_gate_s = c.sh->gate.s; p.sh_up_q = c.sh->up.q; p.sh_up_s = c.sh->up.s;
         p.sh_down_q = c.sh->down.q; p.sh_down_s = c.sh->down.s;
@@ -271,6 +277,7 @@ const char* moe_status_string(int status) {
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait ran out";
         case MOE_ERR_DEVICE_INDEX: return "routed expert id out of range";
+        case MOE_ERR_DEVICE_RANGE: return "MXFP4 scale exponent outside the supported range";
         default: return "unknown status";
     }
 }
@@ -490,6 +497,13 @@ int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const ui
 int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (!ws || ws_bytes < kWsHead) return MOE_ERR_INVALID_ARG;
     return status_of(cudaMemsetAsync(ws, 0, kWsHead, S(stream)));
+}
+
+int moe_mxfp4_scales(const uint8_t* e8, size_t n, uint16_t* s, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!e8 || !s || !ws || ws_bytes < kWsHead || (reinterpret_cast<uintptr_t>(s) & 1u)) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (int st = check_device()) return st;
+    return status_of(launch_mxfp4_scales(e8, n, s, static_cast<int*>(ws), S(stream)));
 }
 
 int moe_device_status(void* ws, size_t ws_bytes, int* status, moe_stream_t stream) {

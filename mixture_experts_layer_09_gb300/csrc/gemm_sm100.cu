@@ -8,9 +8,10 @@
 // backend: expert tier + dense + MLA attention on any Vulkan 1.2 GPU", Correctness and
 // "Grouped scales in the Vulkan kernels"), expanded by producer warps into fp16
 // (nibble - 8) * scale directly in the 128-byte-swizzled K-major layout the tensor core
-// reads; B is the tile's activation rows (fp16), brought in by TMA with the same swizzle;
-// D = A * B^T accumulates in tensor memory (fp32), 128 lanes x N columns, N = tile rows
-// rounded to 16.
+// reads (MXFP4 rows, the fmt=7 format of the same PR: fp16 2v * 2^(e - 128) per e2m1 code,
+// exact, chosen per work item); B is the tile's activation rows (fp16), brought in by TMA with
+// the same swizzle; D = A * B^T accumulates in tensor memory (fp32), 128 lanes x N columns,
+// N = tile rows rounded to 16.
 //
 // Gate/up (moe_gateup_kernel): one CTA per (128 features, token tile); gate and up are two
 // accumulators of 256 columns, so the epilogue forms silu(g) * u (the fused gate+up+silu of
@@ -33,6 +34,7 @@
 #include "async.cuh"
 #include "tcgen05.cuh"
 #include "common.cuh"
+#include "fp4.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -76,6 +78,7 @@ struct GemmK {
     int items_r;          // routed work items (ntile_max * mblk_r); shared items follow
     int items;            // all work items (the gate/up grid)
     int out_mode;         // down: 0 rows (unweighted, dispatch order), 1 weighted slots
+    int fp4_r, fp4_s;     // MXFP4 codes (else int4) in the routed / shared matrices
     int sh_row0;          // B row of the first shared token in tm_s
     const int* tiles;     // [3 * ntile] (expert, first dispatch row, rows)
     const int* n_tiles;
@@ -188,16 +191,25 @@ __device__ __forceinline__ RawK<CPT> load_raw(const uint8_t* qrow, const uint16_
     return r;
 }
 
-// Writes chunks part*CPT .. part*CPT+CPT-1 of `row` into a 128-byte-swizzled K-major tile.
-template <int CPT>
+// Writes chunks part*CPT .. part*CPT+CPT-1 of `row` into a 128-byte-swizzled K-major tile;
+// FP4: the words hold e2m1 codes (the same K order, fp4.cuh).
+template <int CPT, bool FP4>
 __device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int part, const RawK<CPT>& r) {
     const __half2 s2 = __half2half2(__ushort_as_half(r.s));
     uint8_t* rowp = tile + row * 128;
 #pragma unroll
     for (int j = 0; j < CPT; ++j) {
         const int c = part * CPT + j;
-        *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = dequant8(r.q[j], s2);
+        *reinterpret_cast<uint4*>(rowp + ((c ^ (row & 7)) << 4)) = FP4 ? e2m1x8_to_f16(r.q[j], s2) : dequant8(r.q[j], s2);
     }
+}
+
+template <int CPT>
+__device__ __forceinline__ void store_dequant(uint8_t* tile, int row, int part, const RawK<CPT>& r, bool fp4) {
+    if (fp4)
+        store_dequant<CPT, true>(tile, row, part, r);
+    else
+        store_dequant<CPT, false>(tile, row, part, r);
 }
 
 // TMA of a tile's B rows for one K-step: one 128-row box per lane (copies issued by one thread
@@ -319,6 +331,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
         const uint16_t* sa = (w.shared ? p.sa_s : p.sa_r) + grow * (w.K / 32);
         const uint8_t* qb = (w.shared ? p.qb_s : p.qb_r) + grow * (w.K / 2);
         const uint16_t* sb = (w.shared ? p.sb_s : p.sb_r) + grow * (w.K / 32);
+        const bool fp4 = w.shared ? p.fp4_s : p.fp4_r;
         // raw weights kGuPrefetch K-steps ahead in registers; one lane per warp waits for a free
         // stage and one arrives for the warp (after __syncwarp orders the warp's writes)
         RawK<CPT> ra[kGuPrefetch], rb[kGuPrefetch];
@@ -342,8 +355,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
                         break;
                     }
                 }
-                store_dequant<CPT>(stage_a(s, 0), pr, part, ra[d]);
-                store_dequant<CPT>(stage_a(s, 1), pr, part, rb[d]);
+                store_dequant<CPT>(stage_a(s, 0), pr, part, ra[d], fp4);
+                store_dequant<CPT>(stage_a(s, 1), pr, part, rb[d], fp4);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(full_a + s);
@@ -534,6 +547,7 @@ __global__ void __launch_bounds__(kDnThreads, 1) moe_down_kernel(const __grid_co
             const size_t grow = w.shared ? static_cast<size_t>(wrow) : static_cast<size_t>(w.e) * w.M + wrow;
             const uint8_t* qa = (w.shared ? p.qa_s : p.qa_r) + grow * (w.K / 2);
             const uint16_t* sa = (w.shared ? p.sa_s : p.sa_r) + grow * (w.K / 32);
+            const bool fp4 = w.shared ? p.fp4_s : p.fp4_r;
             const int nk = w.K / BK;
             // raw weights kDnPrefetch K-steps ahead in registers; one lane per warp waits for a
             // free stage and one arrives for the warp (after __syncwarp orders its writes)
@@ -554,7 +568,7 @@ __global__ void __launch_bounds__(kDnThreads, 1) moe_down_kernel(const __grid_co
                             break;
                         }
                     }
-                    store_dequant<CPT>(stage_a(s), pr, part, ra[d]);
+                    store_dequant<CPT>(stage_a(s), pr, part, ra[d], fp4);
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(full_a + s);
@@ -757,6 +771,8 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     GemmK g{};
     g.T = p.T;
     g.k = p.k;
+    g.fp4_r = p.fp4_r;
+    g.fp4_s = p.fp4_s;
     g.E = p.E;
     g.tiles = p.tiles;
     g.n_tiles = p.n_tiles;

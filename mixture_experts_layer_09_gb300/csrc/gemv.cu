@@ -12,6 +12,10 @@
 // nibbles per instruction).  The only rounding is the activation's: bf16 hidden values within
 // 2^7 of their group's largest magnitude convert exactly, smaller ones round at 2^-15 of it;
 // h rounds at 2^-15 of its group's largest magnitude.
+// MXFP4 matrices (e2m1 codes, the fmt=7 format of colibri PR #418's Kimi K3 tier) take the same
+// path: a chunk's codes expand to the signed bytes 2v (fp4.cuh), the dot product stays exact,
+// there is no offset term, and the upload-expanded scale 2^(e - 128) multiplies the partial.
+// The format is per matrix set (routed or shared), chosen per stage.
 //
 // Work layout (both kernels): a CTA owns 32 consecutive weight rows of one expert; each of its
 // 8 warps owns 4 of them, with 8 lanes per row splitting the row's chunks, so every 128-bit
@@ -30,6 +34,7 @@
 
 #include "async.cuh"
 #include "common.cuh"
+#include "fp4.cuh"
 #include "internal.h"
 #include "quant.cuh"
 
@@ -94,6 +99,23 @@ __device__ __forceinline__ Nib split_nibbles(const uint4 w) {
         n.hi[m] = (ww[m] >> 4) & 0x0F0F0F0Fu;   // columns 8m + 1, 3, 5, 7
     }
     return n;
+}
+
+// The same split of an MXFP4 chunk: signed bytes 2v of the e2m1 codes (no offset to remove).
+__device__ __forceinline__ Nib split_e2m1(const uint4 w) {
+    Nib n;
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) e2m1x8_to_i8(ww[m], n.lo[m], n.hi[m]);
+    return n;
+}
+
+template <bool FP4>
+__device__ __forceinline__ Nib split_chunk(const uint4 w) {
+    if constexpr (FP4)
+        return split_e2m1(w);
+    else
+        return split_nibbles(w);
 }
 
 // sum over the 32 columns of a chunk of nibble * activation; a = 32 int16 in dp2a order.
@@ -278,7 +300,7 @@ __device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt
 // One slice with staged scales for NB tokens: chunks ks, ks + 8, ... below nch (a slice
 // shorter than KC, as the last or only slice of a short K, ends early; when nch is a multiple
 // of 8 every lane stops at the same chunk).
-template <int MODE, int NB>
+template <int MODE, int NB, bool FP4>
 __device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, int nch,
                                           float (&acc)[Pipe<MODE>::TB][Pipe<MODE>::NMAT]) {
     using P = Pipe<MODE>;
@@ -291,7 +313,7 @@ __device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, i
         float fs[NMAT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
-            nw[m] = split_nibbles(
+            nw[m] = split_chunk<FP4>(
                 *reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB + lrow * kBoxB + (c & 15) * 16));
             fs[m] = f16_to_f32(*reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2));
         }
@@ -303,9 +325,10 @@ __device__ __forceinline__ void stage_dot(const uint8_t* st, int ks, int lrow, i
             for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
             const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
             const float asc = __int_as_float(amv.x);
+            const int off = FP4 ? 0 : 8 * amv.y;  // int4: sum of (n - 8) a = sum n a - 8 sum a
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
-                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - off), fs[m] * asc, acc[b][m]);
         }
     }
 }
@@ -606,14 +629,22 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                 for (int m = 0; m < NMAT; ++m) acc[b][m] = 0.f;
         }
         const bool ws = hd->shared ? ((MODE == 0) ? p.ws_sh_gu : p.ws_sh_d) : ((MODE == 0) ? p.ws_gu : p.ws_d);
+        const bool fp4 = hd->shared ? p.fp4_s : p.fp4_r;
         const int nch = min(P::KC, K - sl * P::KC) / 32;
-        if (ws) {
+        if (ws && !fp4) {
             // staged scales: specialised on the token count
             switch (nb) {
-                case 1: stage_dot<MODE, 1>(st, ks, lrow, nch, acc); break;
-                case 2: stage_dot<MODE, 2>(st, ks, lrow, nch, acc); break;
-                case 3: stage_dot<MODE, 3>(st, ks, lrow, nch, acc); break;
-                default: stage_dot<MODE, 4>(st, ks, lrow, nch, acc); break;
+                case 1: stage_dot<MODE, 1, false>(st, ks, lrow, nch, acc); break;
+                case 2: stage_dot<MODE, 2, false>(st, ks, lrow, nch, acc); break;
+                case 3: stage_dot<MODE, 3, false>(st, ks, lrow, nch, acc); break;
+                default: stage_dot<MODE, 4, false>(st, ks, lrow, nch, acc); break;
+            }
+        } else if (ws) {
+            switch (nb) {
+                case 1: stage_dot<MODE, 1, true>(st, ks, lrow, nch, acc); break;
+                case 2: stage_dot<MODE, 2, true>(st, ks, lrow, nch, acc); break;
+                case 3: stage_dot<MODE, 3, true>(st, ks, lrow, nch, acc); break;
+                default: stage_dot<MODE, 4, true>(st, ks, lrow, nch, acc); break;
             }
         } else {
 #pragma unroll
@@ -624,8 +655,9 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                     float fs[NMAT];
 #pragma unroll
                     for (int m = 0; m < NMAT; ++m) {
-                        nw[m] = split_nibbles(*reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB +
-                                                                              lrow * kBoxB + (c & 15) * 16));
+                        const uint4 wv = *reinterpret_cast<const uint4*>(st + m * P::WMAT + (c >> 4) * 32 * kBoxB +
+                                                                         lrow * kBoxB + (c & 15) * 16);
+                        nw[m] = fp4 ? split_e2m1(wv) : split_nibbles(wv);
                         uint16_t sb;
                         if (ws) {
                             sb = *reinterpret_cast<const uint16_t*>(st + P::OFF_WS + (m * 32 + lrow) * P::GRP * 2 + c * 2);
@@ -651,9 +683,10 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
                             for (int q = 0; q < 4; ++q) av[q] = ap[((c >> 3) * 4 + q) * 8 + (c & 7)];
                             const int2 amv = reinterpret_cast<const int2*>(st + P::OFF_AM)[b * P::GRP + c];
                             const float asc = __int_as_float(amv.x);
+                            const int off = fp4 ? 0 : 8 * amv.y;
 #pragma unroll
                             for (int m = 0; m < NMAT; ++m)
-                                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - 8 * amv.y), fs[m] * asc, acc[b][m]);
+                                acc[b][m] = fmaf(static_cast<float>(dot_nib(nw[m], av) - off), fs[m] * asc, acc[b][m]);
                         }
                     }
                 }

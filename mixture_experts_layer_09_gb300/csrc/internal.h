@@ -83,6 +83,7 @@ struct GemvArgs {
     const uint16_t* up_s;
     const uint8_t* down_q;
     const uint16_t* down_s;
+    int fp4_r, fp4_s;             // MXFP4 codes (else int4) in the routed / shared matrices
     // shared expert (sh_I == 0: none)
     int sh_I;
     const uint8_t* sh_gate_q;
@@ -147,6 +148,7 @@ struct GemmPlan {
     const uint16_t* sh_up_s;
     const uint8_t* sh_down_q;
     const uint16_t* sh_down_s;
+    int fp4_r, fp4_s;             // MXFP4 codes (else int4) in the routed / shared matrices
     // activations / scratch
     const uint16_t* x;            // bf16 [T][H]
     uint16_t* x16;                // fp16 [T*k + T][H]: dispatch-order rows, then token-order rows
@@ -164,6 +166,10 @@ constexpr int kGemmTileN = 256;   // tokens per tile
 int gemm_ntile_max(int n_slots, int E);
 bool gemm_supported(int H, int I, int I_sh);
 cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st);
+
+// MXFP4 upload: fp16 2^(e - 128) per ue8m0 exponent; out-of-range exponents record
+// MOE_ERR_DEVICE_RANGE in *status.
+cudaError_t launch_mxfp4_scales(const uint8_t* e8, size_t n, uint16_t* s, int* status, cudaStream_t st);
 
 // norm.cu: RMSNorm of the layer output into bf16 rows (H % 4 == 0, y 16-byte and gamma/out
 // 8-byte aligned)

@@ -28,7 +28,8 @@ def parse_workload(args) -> gen.Workload:
         if len(v) not in (5, 6):
             raise SystemExit("--shape wants H,I,E,k,T[,I_sh]")
         H, I, E, k, T = v[:5]
-        return gen.Workload(f"H{H}_I{I}_E{E}_k{k}_T{T}", T, H, I, E, k, I_sh=v[5] if len(v) > 5 else 0)
+        return gen.Workload(f"H{H}_I{I}_E{E}_k{k}_T{T}", T, H, I, E, k, I_sh=v[5] if len(v) > 5 else 0,
+                            fmt=args.fmt)
     if args.workload not in gen.WORKLOADS:
         raise SystemExit(f"unknown workload {args.workload}; known: {', '.join(gen.WORKLOADS)}")
     return gen.WORKLOADS[args.workload]
@@ -41,15 +42,15 @@ def upload(torch, moe, wl: gen.Workload, seed: int):
         return (t.view(dtype) if dtype is not None else t).cuda()
 
     def q4(m):
-        return moe.Q4(dev(m.q), dev(m.s.view(np.int16), torch.float16))
+        return moe.upload_q4(m.q, m.s, m.fmt)
 
-    ex = gen.draw_experts(seed, wl.E, wl.H, wl.I)
+    ex = gen.draw_experts(seed, wl.E, wl.H, wl.I, wl.fmt)
     W = moe.Experts(wl.E, wl.H, wl.I, q4(ex.gate), q4(ex.up), q4(ex.down))
     del ex
     W_r = dev(gen.draw_router(seed, wl.E, wl.H).view(np.int16), torch.bfloat16)
     sh = None
     if wl.I_sh:
-        s = gen.draw_shared(seed, wl.H, wl.I_sh)
+        s = gen.draw_shared(seed, wl.H, wl.I_sh, fmt=wl.sh_fmt)
         sh = moe.Shared(wl.I_sh, q4(s.gate), q4(s.up), q4(s.down), dev(s.g.view(np.int16), torch.bfloat16))
     return moe.MoeLayer(W_r, W, sh, wl.k, wl.T)
 
@@ -58,6 +59,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--workload", default="qwen3_30b_decode_t16")
     ap.add_argument("--shape", default="", help="H,I,E,k,T[,I_sh] instead of a named workload")
+    ap.add_argument("--fmt", default="int4", choices=("int4", "mxfp4"), help="routed experts' format (--shape)")
     ap.add_argument("--arm", choices=list(ARMS), default="auto")
     ap.add_argument("--iters", type=int, default=4)
     ap.add_argument("--warmup", type=int, default=3)

@@ -95,6 +95,30 @@ def test_host_argument_checks(L):
                                C.c_void_p(0x10000), 1 << 30, None) == -1   # unknown arm
     assert L.moe_layer_forward(fake, None, fake, C.byref(ok), None, 0, 2, fake, None, None, 0,
                                C.c_void_p(0x10000), 1 << 30, None) == 0    # T = 0
+    # weight formats: unknown format codes are rejected, for the routed and the shared set
+    badfmt = moe.moe_experts(8, 256, 128, q, q, q, 2)
+    assert L.moe_layer_forward(fake, None, fake, C.byref(badfmt), None, 4, 2, fake, None, None, 0,
+                               C.c_void_p(0x10000), 1 << 30, None) == -1
+    sh_bad = moe.moe_shared(64, q, q, q, None, -1)
+    assert L.moe_layer_forward(fake, None, fake, C.byref(ok), C.byref(sh_bad), 4, 2, fake, None, None, 0,
+                               C.c_void_p(0x10000), 1 << 30, None) == -1
+    # MXFP4 scale expansion: null pointers, a short workspace, a misaligned output
+    assert L.moe_mxfp4_scales(None, 16, fake, fake, 4096, None) == -1
+    assert L.moe_mxfp4_scales(fake, 16, fake, fake, 100, None) == -1
+    assert L.moe_mxfp4_scales(fake, 16, C.c_void_p(0x1001), fake, 4096, None) == -1
+    assert L.moe_mxfp4_scales(fake, 0, fake, fake, 4096, None) == 0
+    assert L.moe_status_string(-6).startswith(b"MXFP4 scale exponent")
+
+
+def test_binding_weight_format_checks():
+    # gate/up/down must share one format; the struct carries its code
+    q4 = moe.Q4(None, None, "int4")
+    fp4 = moe.Q4(None, None, "mxfp4")
+    assert moe._fmt_of(fp4, fp4, fp4) == 1 and moe._fmt_of(q4, q4, q4) == 0
+    with pytest.raises(moe.MoeError):
+        moe._fmt_of(q4, fp4, q4)
+    with pytest.raises(moe.MoeError):
+        moe._fmt_of(moe.Q4(None, None, "nf4"))
 
 
 def test_no_cpu_fallback_without_device(L):

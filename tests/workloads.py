@@ -96,7 +96,7 @@ def upload(inp: gen.LayerInputs):
     import mixture_experts_layer_09_gb300 as moe
 
     def q4(m: gen.Q4):
-        return moe.Q4(dev(m.q), dev(m.s.view(np.int16), torch.float16))
+        return moe.upload_q4(m.q, m.s, m.fmt)
 
     ex = inp.experts
     E = moe.Experts(ex.E, ex.H, ex.I, q4(ex.gate), q4(ex.up), q4(ex.down))
