@@ -418,6 +418,27 @@ def time_loop(torch, fn, steps, warmup):
     return e0.elapsed_time(e1) / 1e3
 
 
+def reduce_max(dist, v: float, device) -> float:
+    """The largest of every rank's v: a replicated job takes as long as its slowest rank.  No
+    process group (one rank): v itself."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank: int) -> int:
+    """Seed base of a rank's replicas and inputs: every rank holds independent layers."""
+    return 1000 * rank
+
+
+def job_value(world: int, tokens_per_step: int, steps: int, seconds: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return world * tokens_per_step * steps / seconds
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -430,7 +451,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(local)
     moe.build()
     H, I, E, k, T = WORKLOAD["H"], WORKLOAD["I"], WORKLOAD["E"], WORKLOAD["k"], WORKLOAD["T"]
-    seed0 = 1000 * rank
+    seed0 = rank_seed(rank)
 
     # ---- resident weights: independent layer replicas
     layers = []
@@ -463,11 +484,7 @@ def run_ours(args, rank, world):
         n0 = moe.moe_launch_count()
         dt = time_loop(torch, step, steps, warmup)
         out["launches_per_step"] = (moe.moe_launch_count() - n0) / (steps + warmup)
-        if dist is not None:
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        out["plain_s"] = dt
+        out["plain_s"] = reduce_max(dist, dt, "cuda")
         # CUDA-graph replay of the same steps (one graph per (replica, input) pair)
         graphs = []
         s = torch.cuda.Stream()
@@ -482,11 +499,7 @@ def run_ours(args, rank, world):
                 step(i)
             graphs.append(g)
         dtg = time_loop(torch, lambda i: graphs[i % N_INPUTS].replay(), steps, warmup)
-        if dist is not None:
-            t = torch.tensor([dtg], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dtg = float(t.item())
-        out["graph_s"] = dtg
+        out["graph_s"] = reduce_max(dist, dtg, "cuda")
         # distinct experts per step (routing is the GPU's own output)
         nd = []
         for i in range(N_INPUTS):
@@ -512,11 +525,7 @@ def run_ours(args, rank, world):
                 yh.copy_(y, non_blocking=True)
 
             dte = time_loop(torch, e2e_step, steps, warmup)
-            if dist is not None:
-                t = torch.tensor([dte], device="cuda")
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                dte = float(t.item())
-            out["e2e_s"] = dte
+            out["e2e_s"] = reduce_max(dist, dte, "cuda")
             out["h2d"] = 2 * Tb * H * 2
             out["d2h"] = Tb * H * 4
         return out
@@ -552,7 +561,7 @@ def run_ours(args, rank, world):
     steps = args.steps
     best_s = min(main["plain_s"], main["graph_s"])
     ms_step = 1e3 * best_s / steps
-    value = world * T * steps / best_s
+    value = job_value(world, T, steps, best_s)
     hbm, tc, src = peaks()
     # roofline of the dominant kernel (by device time)
     kern = main["kernels"]
@@ -593,7 +602,7 @@ def run_ours(args, rank, world):
         "prefill": prefill,
         **extra,
         "clocks": main.get("clocks"),
-        "e2e": {"value": world * T * steps / main["e2e_s"], "unit": "tokens/s",
+        "e2e": {"value": job_value(world, T, steps, main["e2e_s"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
     }
     if not args.no_cpu_baseline:
