@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -532,7 +533,8 @@ def run_ours(args, rank, world):
 
     # SM clocks are sampled (nvidia-smi, 200 ms) over the whole measurement phase, which
     # contains the timed region: a region of a few ms alone would fall between two samples.
-    clocks = Clocks(os.path.join(ROOT, "gpurun_out" if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ".",
+    # the samples go to $BENCH_CLOCKS_DIR (default: the temporary directory)
+    clocks = Clocks(os.path.join(os.environ.get("BENCH_CLOCKS_DIR", tempfile.gettempdir()),
                                  f"clocks_bench_r{rank}.csv"), local)
     clocks.start()
     main = measure(T, args.steps, args.warmup, full=True)

@@ -75,7 +75,7 @@ typedef void* moe_stream_t; /* a cudaStream_t */
 enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = -1,     /* null pointer, size out of range, workspace too small */
-    MOE_ERR_UNSUPPORTED = -2,     /* valid request this build does not serve */
+    MOE_ERR_UNSUPPORTED = -2,     /* valid request the library does not serve */
     MOE_ERR_CUDA = -3,            /* a CUDA call or launch failed (no device, bad stream, ...) */
     MOE_ERR_DEVICE_TIMEOUT = -4,  /* a bounded device-side wait ran out (recorded on device) */
     MOE_ERR_DEVICE_INDEX = -5,    /* a routed expert id outside [0, E) (recorded on device) */
