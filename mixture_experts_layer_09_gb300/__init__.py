@@ -215,12 +215,12 @@ def upload_q4(q, s, fmt: str = "int4", device="cuda") -> Q4:
     and raises when an exponent is out of range."""
     import numpy as np
     import torch
+    if fmt not in WFMT:
+        raise MoeError(-1, f"unknown weight format {fmt!r}")
     qd = torch.from_numpy(np.ascontiguousarray(q, dtype=np.uint8)).to(device)
     if fmt == "int4":
         sd = torch.from_numpy(np.ascontiguousarray(s, dtype=np.uint16).view(np.int16)).to(device).view(torch.float16)
         return Q4(qd, sd, "int4")
-    if fmt != "mxfp4":
-        raise MoeError(-1, f"unknown weight format {fmt!r}")
     e8 = torch.from_numpy(np.ascontiguousarray(s, dtype=np.uint8)).to(device)
     sd = torch.empty(e8.shape, dtype=torch.float16, device=device)
     ws = _workspace(4096, device)

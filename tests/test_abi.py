@@ -5,6 +5,7 @@ import ctypes as C
 import os
 import re
 
+import numpy as np
 import pytest
 
 import mixture_experts_layer_09_gb300 as moe
@@ -119,6 +120,8 @@ def test_binding_weight_format_checks():
         moe._fmt_of(q4, fp4, q4)
     with pytest.raises(moe.MoeError):
         moe._fmt_of(moe.Q4(None, None, "nf4"))
+    with pytest.raises(moe.MoeError):
+        moe.upload_q4(np.zeros((1, 32, 16), np.uint8), np.zeros((1, 32, 1), np.uint16), "nf4")
 
 
 def test_no_cpu_fallback_without_device(L):
