@@ -45,3 +45,25 @@ def test_zipf_workload_is_skewed():
     share = np.bincount(ids.ravel(), minlength=inp.wl.E) / ids.size
     assert share[0] > 0.3 and share[0] > 4 * share[-1]
     assert np.all(np.diff(share[:4]) < 0)  # the head of the distribution is strictly ordered
+
+
+def test_algorithmic_bytes_match_the_uploaded_arrays():
+    """The roofline's bytes per expert equal what one expert's three matrices occupy in the
+    layout the kernels stream (codes plus a 2-byte scale per 32 columns), for both formats;
+    the MXFP4 upload turns each exponent byte into a 2-byte scale."""
+    import numpy as np
+
+    sys.path.insert(0, ROOT)
+    import bench
+    from mixture_experts_layer_09_gb300 import inputs as gen
+    for H, I in ((256, 128), (2048, 768), (6144, 2048)):
+        for fmt in ("int4", "mxfp4"):
+            ex = gen.draw_experts(3, 1, H, I, fmt)
+            q_bytes = sum(m.q.nbytes for m in (ex.gate, ex.up, ex.down))
+            s_elems = sum(m.s.size for m in (ex.gate, ex.up, ex.down))
+            assert bench.BYTES_PER_EXPERT(H, I) == q_bytes + 2 * s_elems, (H, I, fmt)
+    # the per-expert figures the measurement plan quotes
+    assert bench.BYTES_PER_EXPERT(2048, 768) == 2_654_208
+    assert bench.BYTES_PER_EXPERT(6144, 2048) == 21_233_664
+    assert bench.BYTES_PER_EXPERT(2048, 1408) == 4_866_048
+    assert np.isclose(bench.BYTES_PER_EXPERT(2048, 5632), 19_464_192)
