@@ -534,3 +534,30 @@ def test_mxfp4_generator_ranges():
     assert m.s.min() >= lo and m.s.max() <= hi and len(np.unique(m.s)) == hi - lo + 1
     # the codes are the int4 set's nibbles: same stream
     assert np.array_equal(m.q, gen.draw_q4(0, gen.TAG_GATE, 2, 32, 256).q)
+
+
+def test_mxfp4_dequant_by_numpy_table(oracle_lib):
+    # unpack the codes with numpy bit operations and the OCP value table, scale by 2^(e-127)
+    d = _gold("mxfp4_decode.json")
+    table = np.array(d["e2m1_values"], dtype=np.float64)
+    m = gen.draw_mxfp4(9, gen.TAG_GATE, 1, 32, 96)
+    q, e8 = m.q[0], m.s[0]
+    codes = np.empty((32, 96), dtype=np.int64)
+    codes[:, 0::2], codes[:, 1::2] = q & 0xF, q >> 4
+    ref = table[codes] * np.repeat(np.ldexp(1.0, e8.astype(np.int64) - 127), 32, axis=1)
+    assert np.array_equal(oracle_lib.dequant_mxfp4(q, e8, 32, 96), ref)
+
+
+def test_mxfp4_mlp_is_dense_restatement(oracle_lib):
+    H, I = 64, 96
+    ex = gen.draw_experts(3, 1, H, I, gen.FMT_MXFP4)
+    x = gen.bf16_bits(gen.rng(4).normal(size=H))
+    o = oracle_lib.expert_row(x, (ex.gate.q[0], ex.gate.s[0]), (ex.up.q[0], ex.up.s[0]),
+                              (ex.down.q[0], ex.down.s[0]), H, I, "mxfp4")
+    Wg = oracle_lib.dequant_mxfp4(ex.gate.q[0], ex.gate.s[0], I, H)
+    Wu = oracle_lib.dequant_mxfp4(ex.up.q[0], ex.up.s[0], I, H)
+    Wd = oracle_lib.dequant_mxfp4(ex.down.q[0], ex.down.s[0], H, I)
+    xf = gen.bf16_to_f32(x).astype(np.float64)
+    g, u = Wg @ xf, Wu @ xf
+    ref = Wd @ (g / (1 + np.exp(-g)) * u)
+    assert np.allclose(o, ref, rtol=1e-12, atol=1e-12)
