@@ -13,7 +13,8 @@
  *      nibble - 8) with one fp16 scale per 32 K-columns: gate+up, silu(gate)*up,
  *      down [colibri PR #418 "Vulkan backend: expert tier + dense + MLA
  *      attention on any Vulkan 1.2 GPU", Summary, Correctness and "Grouped
- *      scales in the Vulkan kernels"];
+ *      scales in the Vulkan kernels"]; or over MXFP4 weights (e2m1 codes, one
+ *      ue8m0 scale per 32 K-columns, the same PR's fmt=7), per expert set;
  *   4. weighted combine onto the residual plus an optional shared expert scaled
  *      by sigmoid(x . g) [daScript PR #3988, decode span commit: DecCombineSh;
  *      the combine-folded residual commit: shared row, then the slots in
@@ -139,8 +140,9 @@ MOE_API const char* moe_version(void);
  *   x       bf16 [T][H]        W_r bf16 [E][H]        g bf16 [H] or NULL
  *   logits  fp32 [T][E + (g != NULL)], fp32 accumulation of bf16 products.
  * T <= 32 runs a GEMV; larger T runs a tcgen05 GEMM when H % 64 == 0,
- * E <= 256 and x, W_r, g are 16-byte aligned (else a tiled fp32 GEMM).  The tensor-core kernel's bounded waits
- * cannot report a timeout through this call (it has no workspace status word).
+ * E <= 256 and x, W_r, g are 16-byte aligned (else a tiled fp32 GEMM).  The
+ * tensor-core kernel's bounded waits cannot report a timeout through this call
+ * (it has no workspace status word).
  * T = 0 is a no-op. */
 MOE_API int moe_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
                       int T, int H, int E, float* logits, moe_stream_t stream);
