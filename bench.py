@@ -1,20 +1,29 @@
 #!/usr/bin/env python
-"""Benchmark of the routed MoE layer on one GB300: tokens/s and us/layer.
+"""Benchmark of the routed MoE layer on one GB300: tokens/s and us/layer against the roofline.
 
-Workload: the Qwen3-30B-A3B-shaped decode layer (H=2048, I=768, E=128, top-k=8, no shared
-expert, int4 nibble-8 experts with fp16 scales per 32 columns), batch T=16 tokens, synthetic
-seeded inputs.  A step = one moe_layer_forward call (router logits, softmax top-k, dispatch,
-fused int4 expert MLP with the combine in the down projection) on one batch.  Weights stay
-resident in HBM; L2 reuse between steps is defeated by cycling 4 independent layer replicas
-(340 MB of experts each, 4 x 340 MB > 4 x L2) and 16 distinct input batches.
+Headline workload: the Qwen1.5-MoE-A2.7B-shaped prefill layer with its sigmoid-gated shared
+expert (H=2048, routed I=1408, E=60, top-k=4, shared I_sh=5632, int4 nibble-8 experts with fp16
+scales per 32 columns), T=4096 tokens -- the largest configuration, where the layer is a
+grouped GEMM bound by the tensor cores.  A step = one moe_layer_forward call (router logits,
+softmax top-k, dispatch, grouped int4 gate/up + SwiGLU and down GEMMs, combine onto the
+residual) on one batch.  Weights stay resident in HBM; L2 reuse between steps is defeated by
+cycling 2 independent layer replicas (311 MB of experts each, far above the 129 MB L2) and 4
+distinct token batches.  Each step is timed by its own CUDA-event pair on the launching stream
+(the median and the 10th / 90th percentiles are reported beside the whole region's mean).
 
-Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle instead, on a
-bounded sample of the same workload.  Multi-GPU (torchrun) runs independent replicas, one per
+The line also carries, as flat numbers in ``config``, the decode layers (Qwen3-30B-A3B-shaped
+T=1/4/16 and GLM-class k=8/32 T=1/8, bound by HBM), the T=512 prefill layer, the router +
+dispatch sweep and the skewed tiny layer; the fp64 CPU oracle is timed on the host cores, all
+of them and one thread.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle instead, on bounded
+token slices of the same workload.  Multi-GPU (torchrun) runs independent replicas, one per
 rank: the layer has no cross-GPU exchange, so no collective touches the data path.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -32,20 +41,30 @@ import numpy as np  # noqa: E402
 from mixture_experts_layer_09_gb300 import inputs as gen  # noqa: E402
 
 METRIC = "MoE-layer tokens/s & us/layer at 1 GB300; % of HBM (decode) / TC (prefill) roof"
-WORKLOAD = dict(name="qwen3_30b_a3b_decode_moe_layer", H=2048, I=768, E=128, k=8, T=16)
-SWEEP_T = (1, 4)
-N_REPLICAS = 4
-N_INPUTS = 16
+HEADLINE = dict(name="qwen15_moe_a2.7b_prefill_layer", H=2048, I=1408, E=60, k=4, I_sh=5632, T=4096)
+DECODE = dict(name="qwen3_30b_a3b_decode_moe_layer", H=2048, I=768, E=128, k=8, T=(1, 4, 16))
+N_PREFILL_REPLICAS, N_PREFILL_INPUTS = 2, 4
+N_DECODE_REPLICAS, N_DECODE_INPUTS = 4, 16
 BYTES_PER_EXPERT = lambda H, I: 3 * (H * I // 2) + 3 * (H * I // 32) * 2  # noqa: E731
 
 
 def peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
-    return 6800.0, 1900.0, "fallback"
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), \
+            "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def prefill_flops(T, H, I, E, k, I_sh):
+    """FLOPs of one prefill layer call: the two grouped GEMMs (routed and shared rows) and the
+    router logits (E rows plus the shared gate row)."""
+    gateup = 2.0 * (T * k * H * 2 * I + T * H * 2 * I_sh)
+    down = 2.0 * (T * k * I * H + T * I_sh * H)
+    return {"gemm_gateup": gateup, "gemm_down": down, "layer": gateup + down + 2.0 * T * H * (E + 1)}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -94,23 +113,45 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ----------------------------------------------------------------------------- reference arm
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_slices(n_tokens, seconds, threads, wl_dict=HEADLINE, seed=0):
+    """The fp64 oracle as it stands, on consecutive token slices of a headline-shaped batch (each
+    slice a batch of its own: routing, experts, shared expert and combine of those tokens), until
+    about `seconds` of CPU time.  Returns (tokens/s, tokens, seconds, threads used, slices)."""
+    import oracle
+    oracle.build()
+    oracle.set_threads(threads)
+    w = wl_dict
+    wl = gen.Workload(w["name"], n_tokens, w["H"], w["I"], w["E"], w["k"], I_sh=w.get("I_sh", 0), seed=seed)
+    base = gen.draw_layer(wl)
+    n_tok, dt, b = 0, 0.0, 0
+    while b == 0 or dt < seconds:
+        inp = dataclasses.replace(base, x=gen.draw_x(seed + 3000 + b, n_tokens, w["H"])) if b else base
+        t0 = time.perf_counter()
+        oracle.layer_forward(inp)
+        dt += time.perf_counter() - t0
+        n_tok += n_tokens
+        b += 1
+    return n_tok / dt, n_tok, dt, oracle.get_threads(), b
+
 
 def run_reference(args, rank):
-    """The fp64 CPU oracle as it stands, timed on the host cores: each step is one token of
-    the benchmark batch (routing of the whole batch, then that token's experts and combine)."""
+    """The fp64 CPU oracle as it stands, timed on every host core this process may use: each
+    step is one slice of 8 tokens of the headline workload, run through the whole layer."""
     if rank != 0:
         return
     import oracle
     oracle.build()
-    wl = gen.Workload(WORKLOAD["name"], WORKLOAD["T"], WORKLOAD["H"], WORKLOAD["I"], WORKLOAD["E"], WORKLOAD["k"])
-    inp = gen.draw_layer(wl)
-    T = wl.T
+    threads = oracle.default_threads()
+    oracle.set_threads(threads)
+    w, n = HEADLINE, 8
+    base = gen.draw_layer(gen.Workload(w["name"], n, w["H"], w["I"], w["E"], w["k"], I_sh=w["I_sh"]))
+    slices = [dataclasses.replace(base, x=gen.draw_x(3000 + i, n, w["H"]),
+                                  residual=gen.draw_residual(3100 + i, n, w["H"])) for i in range(4)]
 
     def step(i):
-        mask = np.zeros(T, dtype=np.uint8)
-        mask[i % T] = 1
-        oracle.layer_forward(inp, token_mask=mask)
+        oracle.layer_forward(slices[i % len(slices)])
 
     for i in range(args.warmup):
         step(i)
@@ -118,24 +159,87 @@ def run_reference(args, rank):
     for i in range(args.steps):
         step(i)
     dt = time.perf_counter() - t0
-    tps = args.steps / dt
+    tps = n * args.steps / dt
+    sample = f"{args.steps} slices of {n} tokens of the T={w['T']}-token workload, {threads} threads"
     line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "impl": "reference", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{wl.name} H={wl.H} I={wl.I} E={wl.E} k={wl.k} T={wl.T}",
-                       "impl_note": "fp64 C oracle, single thread"},
-            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} steps of 1 token of the T={T} batch"},
+            "config": {"workload": f"{w['name']} H={w['H']} I={w['I']} E={w['E']} k={w['k']} I_sh={w['I_sh']} "
+                                   f"T={w['T']}",
+                       "impl_note": f"fp64 C oracle on {threads} host threads"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-# ----------------------------------------------------------------------------- our arm
+# ----------------------------------------------------------------------------- timing
+
+def timed_steps(torch, fn, steps, warmup, dist=None):
+    """W untimed warm-up calls, then exactly `steps` calls, each between its own CUDA events on
+    the current stream, the region bracketed by a barrier and a synchronize on both sides.
+    Returns total seconds (max over ranks) and per-call microseconds."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record()
+    for i in range(steps):
+        fn(warmup + i)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    per = [1e3 * ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total = ev[0].elapsed_time(ev[steps]) / 1e3
+    return reduce_max(dist, total, "cuda"), per
+
+
+def summary(per_us):
+    a = np.asarray(per_us, dtype=np.float64)
+    return {"median_us": float(np.median(a)), "p10_us": float(np.percentile(a, 10)),
+            "p90_us": float(np.percentile(a, 90)), "mean_us": float(a.mean()), "calls": int(a.size)}
+
+
+def graph_steps(torch, step, n_graphs, steps, warmup):
+    """The same calls captured as CUDA graphs (one per input index) and replayed."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(0)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graphs = []
+    for i in range(n_graphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(i)
+        graphs.append(g)
+    _, per = timed_steps(torch, lambda i: graphs[i % n_graphs].replay(), steps, warmup)
+    del graphs
+    return per
+
+
+def kernel_times(torch, moe, step, steps):
+    """Per-kernel device time: the library's CUDA-event pairs around each of its launches, on
+    the launching stream.  {name: (total ms, launches)}."""
+    moe.moe_profile_enable(True)
+    for i in range(steps):
+        step(i)
+    torch.cuda.synchronize()
+    kern = moe.moe_profile_read()
+    moe.moe_profile_enable(False)
+    return kern
+
+
+# ----------------------------------------------------------------------------- ncu traffic
 
 # DRAM traffic of a kernel from an ncu capture, valid while the sources it was built from are
 # unchanged: profiles/dram_traffic.txt holds lines "kernel bytes_per_unit unit sha256 note", the
-# hash taken over KERNEL_SOURCES by source_hash(); the GEMV kernels' unit is one distinct expert
-# streamed by the launch, so a launch's traffic is bytes_per_unit x its distinct experts.
+# hash taken over KERNEL_SOURCES by source_hash(); unit "expert" scales by the distinct experts a
+# launch streamed, unit "launch" is the bench's launch as captured.
 KERNEL_SOURCES = {
     "gateup_gemv": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
     "down_gemv_combine": ("gemv.cu", "quant.cuh", "async.cuh", "common.cuh", "fp4.cuh", "internal.h"),
@@ -153,7 +257,7 @@ def source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def dram_traffic(kernel, units):
+def dram_traffic(kernel, units=1.0):
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if kernel not in KERNEL_SOURCES or not os.path.exists(p):
         return None
@@ -166,59 +270,117 @@ def dram_traffic(kernel, units):
     return None
 
 
-def time_layer(torch, layer, xs, steps, warmup, ids):
-    """CUDA-event time per layer call over `steps` calls cycling the inputs `xs`, and the mean
-    number of distinct experts those calls routed to."""
-    T, H = xs[0].shape
-    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+# ----------------------------------------------------------------------------- secondary workloads
 
-    def step(i):
-        layer.forward(xs[i % len(xs)], None, y=y, topk_ids_out=ids)
-
-    dt = time_loop(torch, step, steps, warmup)
-    nd = []
-    for i in range(len(xs)):
-        step(i)
-        nd.append(int(torch.unique(ids).numel()))
-    return 1e6 * dt / steps, float(np.mean(nd))
+def _to_dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
 
 
-def measure_norm(torch, moe, args, layers, T, H):
-    """The decode layer with its RMSNorm output (moe_layer_forward_norm) over the same cycled
-    replicas and inputs as the headline: us/layer with the extra pass."""
+def measure_decode(torch, moe, args, seed0):
+    """Qwen3-30B-A3B-shaped decode layers, T = 1, 4, 16: 4 replicas of 340 MB cycled with 16
+    input batches; median of per-call CUDA-event times, plain launches and CUDA-graph replay."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    hbm = peaks()[0]
+    D = DECODE
+    H, I, E, k = D["H"], D["I"], D["E"], D["k"]
+    layers = [upload(torch, moe, gen.Workload("d", max(D["T"]), H, I, E, k), seed0 + rep)
+              for rep in range(N_DECODE_REPLICAS)]
+    out, kern16 = {}, None
+    for T in D["T"]:
+        xs = [_to_dev(torch, gen.draw_x(seed0 + 500 + i, T, H)) for i in range(N_DECODE_INPUTS)]
+        rs = [_to_dev(torch, gen.draw_residual(seed0 + 700 + i, T, H)) for i in range(N_DECODE_INPUTS)]
+        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+
+        def step(i):
+            layers[i % N_DECODE_REPLICAS].forward(xs[i % N_DECODE_INPUTS], rs[i % N_DECODE_INPUTS], y=y,
+                                                  topk_ids_out=ids)
+
+        n = max(50, args.steps)
+        _, per = timed_steps(torch, step, n, args.warmup)
+        perg = graph_steps(torch, step, N_DECODE_INPUTS, n, args.warmup)
+        nd = []
+        for i in range(N_DECODE_INPUTS):
+            step(i)
+            nd.append(int(torch.unique(ids).numel()))
+        nd = float(np.mean(nd))
+        s, sg = summary(per), summary(perg)
+        us = min(s["median_us"], sg["median_us"])
+        layer_bytes = nd * BYTES_PER_EXPERT(H, I) + E * H * 2 + T * H * (2 + 2 + 4)
+        out[f"T={T}"] = {"us_per_layer": us, "plain_median_us": s["median_us"], "graph_median_us": sg["median_us"],
+                         "p10_us": s["p10_us"], "p90_us": s["p90_us"], "tokens_per_s": T / (us * 1e-6),
+                         "mean_distinct_experts": nd, "layer_bytes": layer_bytes,
+                         "hbm_frac": layer_bytes / (us * 1e-6) / 1e9 / hbm}
+        if T == 16:
+            kern16 = kernel_times(torch, moe, step, n)
+            kb = {"gateup_gemv": nd * (2 * I * H // 2 + 2 * I * (H // 32) * 2) + T * H * 2 + T * (H // 32) * 8
+                  + T * k * I * 4,
+                  "down_gemv_combine": nd * (H * I // 2 + H * (I // 32) * 2) + T * k * I * 2
+                  + T * k * (I // 32) * 8 + T * H * 2 + T * H * 4}
+            kf = {}
+            for name, b in kb.items():
+                if name in kern16:
+                    kus = 1e3 * kern16[name][0] / max(kern16[name][1], 1)
+                    kf[name] = {"us": kus, "bytes": b, "hbm_frac": b / (kus * 1e-6) / 1e9 / hbm}
+            out["T=16"]["kernels"] = kf
+            out["T=16"]["kernels_us_per_step"] = {nm: 1e3 * v[0] / n for nm, v in kern16.items()}
+    del layers
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_norm(torch, moe, args, seed0):
+    """The T=16 decode layer with its RMSNorm output (moe_layer_forward_norm)."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    D = DECODE
+    H, T = D["H"], 16
+    layers = [upload(torch, moe, gen.Workload("d", T, H, D["I"], D["E"], D["k"]), seed0 + rep)
+              for rep in range(N_DECODE_REPLICAS)]
     gamma = torch.from_numpy(gen.bf16_bits(gen.rng(23, H).normal(1.0, 0.1, size=H).astype(np.float32))
                              .view(np.int16)).view(torch.bfloat16).cuda()
-    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
-    xs = [to(gen.draw_x(1500 + i, T, H)) for i in range(N_INPUTS)]
+    xs = [_to_dev(torch, gen.draw_x(1500 + i, T, H)) for i in range(N_DECODE_INPUTS)]
     y = torch.empty((T, H), dtype=torch.float32, device="cuda")
     yn = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
 
     def step(i):
-        layers[i % len(layers)].forward(xs[i % N_INPUTS], None, y=y, norm_gamma=gamma, eps=1e-6, y_norm=yn)
+        layers[i % len(layers)].forward(xs[i % N_DECODE_INPUTS], None, y=y, norm_gamma=gamma, eps=1e-6, y_norm=yn)
 
-    steps = max(10, args.steps // 2)
-    dt = time_loop(torch, step, steps, args.warmup)
-    return {"us_per_layer_with_rmsnorm": 1e6 * dt / steps, "tokens_per_s": T * steps / dt}
+    _, per = timed_steps(torch, step, max(50, args.steps), args.warmup)
+    del layers
+    torch.cuda.empty_cache()
+    us = summary(per)["median_us"]
+    return {"us_per_layer_with_rmsnorm": us, "tokens_per_s": T / (us * 1e-6)}
 
 
 def measure_glm(torch, moe, args):
     """GLM-class decode layers (H=6144, I=2048, E=256, all experts resident: 5.4 GB, far above
     L2), k=8 and k=32, T=1 and T=8, 8 distinct inputs cycled so that routing changes."""
     from mixture_experts_layer_09_gb300.run_case import upload
-    hbm, _, _ = peaks()
+    hbm = peaks()[0]
     H, I, E = 6144, 2048, 256
     bpe = BYTES_PER_EXPERT(H, I)
     out = {"workload": f"glm_class_decode_moe_layer H={H} I={I} E={E}", "bytes_per_expert": bpe}
     base = upload(torch, moe, gen.Workload("g", 8, H, I, E, 8), 70)
-    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
     for k in (8, 32):
         for T in (1, 8):
             layer = moe.MoeLayer(base.W_r, base.experts, None, k, T)
-            xs = [to(gen.draw_x(1300 + i, T, H)) for i in range(8)]
+            xs = [_to_dev(torch, gen.draw_x(1300 + i, T, H)) for i in range(8)]
             ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
-            us, nd = time_layer(torch, layer, xs, max(10, args.steps // 2), args.warmup, ids)
-            gbs = (nd * bpe + E * H * 2 + T * H * 8) / (us * 1e-6) / 1e9
-            out[f"k={k},T={T}"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6), "mean_distinct_experts": nd,
+            y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+
+            def step(i):
+                layer.forward(xs[i % 8], None, y=y, topk_ids_out=ids)
+
+            _, per = timed_steps(torch, step, max(50, args.steps), args.warmup)
+            nd = []
+            for i in range(8):
+                step(i)
+                nd.append(int(torch.unique(ids).numel()))
+            nd = float(np.mean(nd))
+            s = summary(per)
+            gbs = (nd * bpe + E * H * 2 + T * H * 8) / (s["median_us"] * 1e-6) / 1e9
+            out[f"k={k},T={T}"] = {"us_per_layer": s["median_us"], "p10_us": s["p10_us"], "p90_us": s["p90_us"],
+                                   "tokens_per_s": T / (s["median_us"] * 1e-6), "mean_distinct_experts": nd,
                                    "hbm_gbs": gbs, "hbm_frac": gbs / hbm}
     del base
     torch.cuda.empty_cache()
@@ -228,8 +390,9 @@ def measure_glm(torch, moe, args):
 def measure_router_sweep(torch, moe, args):
     """Router + dispatch sweep: bf16 logits ~N(0,1)*2, k=8, E in {32..256}, T in {1..16384}; each
     timed call (moe_router_topk then moe_dispatch) follows an untimed write of 256 MB, so L2
-    holds nothing of it.  Algorithmic bytes: T*E*2 + T*k*8 + T*k*12 + (E+1)*4."""
-    hbm, _, _ = peaks()
+    holds nothing of it; the split per kernel comes from a second pass with per-launch events.
+    Algorithmic bytes: T*E*2 + T*k*8 + T*k*12 + (E+1)*4."""
+    hbm = peaks()[0]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     k, iters = 8, 20
     out = {}
@@ -244,34 +407,44 @@ def measure_router_sweep(torch, moe, args):
             inv = torch.empty(T * k, dtype=torch.int32, device="cuda")
             ws = torch.zeros(moe.moe_dispatch_workspace_size(T, k, E), dtype=torch.uint8, device="cuda")
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            tot = 0.0
-            for i in range(iters + 3):
-                flush.fill_(i & 0xFF)
-                e0.record()
-                moe.moe_router_topk(L, E, k, ids, w)
+
+            def call(variant=False):
+                if variant:
+                    moe.moe_router_topk_v(L, E, k, ids, w, sel_bias=bias, renormalize=False, scale=2.5)
+                else:
+                    moe.moe_router_topk(L, E, k, ids, w)
                 moe.moe_dispatch(ids, E, counts, offsets, perm, inv, ws)
-                e1.record()
-                torch.cuda.synchronize()
-                if i >= 3:
-                    tot += e0.elapsed_time(e1) * 1e3
-            us = tot / iters
-            gbs = (T * E * 2 + T * k * 8 + T * k * 12 + (E + 1) * 4) / (us * 1e-6) / 1e9
-            out[f"E={E},T={T}"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm}
-            if E == 256 and T == 16384:
-                # the router variant: selection bias, weights not renormalised, scaled
-                bias = torch.from_numpy(gen.rng(6, E).normal(0.0, 0.5, size=E).astype(np.float32)).cuda()
-                tot = 0.0
+
+            def timed(variant=False):
+                per = []
                 for i in range(iters + 3):
                     flush.fill_(i & 0xFF)
                     e0.record()
-                    moe.moe_router_topk_v(L, E, k, ids, w, sel_bias=bias, renormalize=False, scale=2.5)
-                    moe.moe_dispatch(ids, E, counts, offsets, perm, inv, ws)
+                    call(variant)
                     e1.record()
                     torch.cuda.synchronize()
                     if i >= 3:
-                        tot += e0.elapsed_time(e1) * 1e3
-                us = tot / iters
-                gbs = (T * E * 2 + E * 4 + T * k * 8 + T * k * 12 + (E + 1) * 4) / (us * 1e-6) / 1e9
+                        per.append(e0.elapsed_time(e1) * 1e3)
+                return float(np.median(per))
+
+            bias = None
+            us = timed()
+            moe.moe_profile_enable(True)
+            for i in range(iters):
+                flush.fill_(i & 0xFF)
+                call()
+            torch.cuda.synchronize()
+            kern = moe.moe_profile_read()
+            moe.moe_profile_enable(False)
+            ab = T * E * 2 + T * k * 8 + T * k * 12 + (E + 1) * 4
+            gbs = ab / (us * 1e-6) / 1e9
+            out[f"E={E},T={T}"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm,
+                                   "kernels_us": {n: 1e3 * v[0] / iters for n, v in kern.items()}}
+            if E == 256 and T == 16384:
+                # the router variant: selection bias, weights not renormalised, scaled
+                bias = torch.from_numpy(gen.rng(6, E).normal(0.0, 0.5, size=E).astype(np.float32)).cuda()
+                us = timed(True)
+                gbs = (ab + E * 4) / (us * 1e-6) / 1e9
                 out[f"E={E},T={T},bias,unnormalised,scale=2.5"] = {"us": us, "gbs": gbs, "hbm_frac": gbs / hbm}
     del flush
     return out
@@ -280,14 +453,14 @@ def measure_router_sweep(torch, moe, args):
 def measure_skewed_layer(torch, moe, args):
     """Tiny-layer shape at T=8192 with Zipf(1.1)-skewed expert popularity (bias channel): both
     roofs reported; the weights (8 experts, 0.4 MB) stay in L2 by nature."""
-    hbm, tc, _ = peaks()
+    hbm, tc, _, _ = peaks()
     wl = gen.WORKLOADS["tiny_zipf_t8192"]
     inp = gen.draw_layer(wl)
-    W_r, Ed = upload_layer(torch, moe, inp)
-    layer = moe.MoeLayer(W_r, Ed, None, wl.k, wl.T)
-    x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).cuda()
-    ids = torch.empty((wl.T, wl.k), dtype=torch.int32, device="cuda")
-    us, _ = time_layer(torch, layer, [x], max(10, args.steps // 2), args.warmup, ids)
+    layer = upload_inputs(torch, moe, inp)
+    x = _to_dev(torch, inp.x)
+    y = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+    _, per = timed_steps(torch, lambda i: layer.forward(x, None, y=y), max(50, args.steps), args.warmup)
+    us = summary(per)["median_us"]
     flops = wl.T * (wl.k * 6 * wl.H * wl.I + 2 * wl.E * wl.H)
     act_bytes = wl.T * wl.H * (2 + 4)
     return {"workload": f"tiny_zipf_t8192 H={wl.H} I={wl.I} E={wl.E} k={wl.k} T={wl.T} (Zipf 1.1 popularity)",
@@ -301,122 +474,54 @@ def measure_mxfp4(torch, moe, args):
     the Qwen3-30B-A3B-shaped decode layer at T=16 (2 replicas of 340 MB cycled with 8 inputs)
     and the Qwen1.5-MoE-A2.7B-shaped prefill layer at T=4096 (2 replicas of 300 MB)."""
     from mixture_experts_layer_09_gb300.run_case import upload
-    hbm, tc, _ = peaks()
-    to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
+    hbm, tc, _, _ = peaks()
     out = {}
     H, I, E, k, T = 2048, 768, 128, 8, 16
     layers = [upload(torch, moe, gen.Workload("m", T, H, I, E, k, fmt=gen.FMT_MXFP4), 80 + r) for r in range(2)]
-    xs = [to(gen.draw_x(1700 + i, T, H)) for i in range(8)]
+    xs = [_to_dev(torch, gen.draw_x(1700 + i, T, H)) for i in range(8)]
     y = torch.empty((T, H), dtype=torch.float32, device="cuda")
     ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
 
     def step(i):
         layers[i % 2].forward(xs[i % 8], None, y=y, topk_ids_out=ids)
 
-    steps = max(10, args.steps // 2)
-    dt = time_loop(torch, step, steps, args.warmup)
+    _, per = timed_steps(torch, step, max(50, args.steps), args.warmup)
     nd = []
     for i in range(8):
         step(i)
         nd.append(int(torch.unique(ids).numel()))
-    us = 1e6 * dt / steps
+    us = summary(per)["median_us"]
     gbs = (np.mean(nd) * BYTES_PER_EXPERT(H, I) + E * H * 2 + T * H * 8) / (us * 1e-6) / 1e9
     out["qwen3_30b_decode_t16_mxfp4"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
                                          "mean_distinct_experts": float(np.mean(nd)), "hbm_gbs": gbs,
                                          "hbm_frac": gbs / hbm}
     del layers
-    P = PREFILL
-    T = 4096
+    P = HEADLINE
+    T = P["T"]
     layers = [upload(torch, moe, gen.Workload("mp", T, P["H"], P["I"], P["E"], P["k"], I_sh=P["I_sh"],
                                               fmt=gen.FMT_MXFP4), 90 + r) for r in range(2)]
-    xs = [to(gen.draw_x(1900 + i, T, P["H"])) for i in range(4)]
+    xs = [_to_dev(torch, gen.draw_x(1900 + i, T, P["H"])) for i in range(4)]
     y = torch.empty((T, P["H"]), dtype=torch.float32, device="cuda")
-
-    def pstep(i):
-        layers[i % 2].forward(xs[i % 4], None, y=y)
-
-    dt = time_loop(torch, pstep, steps, args.warmup)
-    us = 1e6 * dt / steps
-    Hh, Ii, kk, Ish = P["H"], P["I"], P["k"], P["I_sh"]
-    flops = 2.0 * T * (kk * 3 * Hh * Ii + 3 * Hh * Ish + Hh * (P["E"] + 1))
+    _, per = timed_steps(torch, lambda i: layers[i % 2].forward(xs[i % 4], None, y=y), max(20, args.steps // 2),
+                         args.warmup)
+    us = summary(per)["median_us"]
+    fl = prefill_flops(T, P["H"], P["I"], P["E"], P["k"], P["I_sh"])["layer"]
     out["qwen15_prefill_t4096_mxfp4"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
-                                         "layer_tflops": flops / (us * 1e-6) / 1e12,
-                                         "layer_tc_frac": flops / (us * 1e-6) / 1e12 / tc}
+                                         "layer_tflops": fl / (us * 1e-6) / 1e12,
+                                         "layer_tc_frac": fl / (us * 1e-6) / 1e12 / tc}
     del layers
     torch.cuda.empty_cache()
     return out
 
 
-PREFILL = dict(name="qwen15_moe_a2.7b_prefill_layer", H=2048, I=1408, E=60, k=4, I_sh=5632, T=(4096, 512))
-
-
-def measure_prefill(torch, moe, args):
-    """Prefill layer (grouped GEMM arm, tensor-core bound): us/layer, tokens/s and the fraction
-    of the bf16 dense peak that the layer and its two GEMMs reach."""
-    from mixture_experts_layer_09_gb300.run_case import upload
-    P = PREFILL
-    _, tc, src = peaks()
-    res = {"workload": f"{P['name']} H={P['H']} I={P['I']} E={P['E']} k={P['k']} I_sh={P['I_sh']}"}
-    reps = 2  # 2 x 300 MB of int4 weights cycled: more than L2
-    layers = [upload(torch, moe, gen.Workload("p", max(P["T"]), P["H"], P["I"], P["E"], P["k"], I_sh=P["I_sh"]),
-                     50 + r) for r in range(reps)]
-    H, I, k, I_sh = P["H"], P["I"], P["k"], P["I_sh"]
-    for T in P["T"]:
-        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()  # noqa: E731
-        xs = [to(gen.draw_x(900 + i, T, H)) for i in range(4)]
-        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
-
-        def step(i):
-            layers[i % reps].forward(xs[i % 4], None, y=y)
-
-        steps = max(10, args.steps // 2)
-        dt = time_loop(torch, step, steps, args.warmup)
-        moe.moe_profile_enable(True)
-        time_loop(torch, step, steps, 0)
-        kern = moe.moe_profile_read()
-        moe.moe_profile_enable(False)
-        us = 1e6 * dt / steps
-        fl = {"gemm_gateup": 2.0 * (T * k * H * 2 * I + T * H * 2 * I_sh),
-              "gemm_down": 2.0 * (T * k * I * H + T * I_sh * H)}
-        layer_flops = sum(fl.values()) + 2.0 * T * H * (P["E"] + 1)
-        kus = {n: 1e3 * v[0] / steps for n, v in kern.items()}
-        gem = {n: {"us": kus[n], "tflops": fl[n] / (kus[n] * 1e-6) / 1e12,
-                   "frac": fl[n] / (kus[n] * 1e-6) / 1e12 / tc} for n in fl if n in kus}
-        res[f"T={T}"] = {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
-                         "layer_tflops": layer_flops / (us * 1e-6) / 1e12,
-                         "layer_tc_frac": layer_flops / (us * 1e-6) / 1e12 / tc,
-                         "gemm": gem, "kernels_us": kus}
-    res["peak_tflops"] = tc
-    res["peak_source"] = f"bf16 dense burst, {src} (the MMAs take fp16 operands: same dense rate)"
-    del layers
-    torch.cuda.empty_cache()
-    return res
-
-
-def upload_layer(torch, moe, inp):
-    def dev(a, dtype=None):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t.view(dtype) if dtype is not None else t).cuda()
-
+def upload_inputs(torch, moe, inp):
+    """A MoeLayer from drawn layer inputs (routed experts only)."""
     def q4(m):
         return moe.upload_q4(m.q, m.s, m.fmt)
 
     ex = inp.experts
     E = moe.Experts(ex.E, ex.H, ex.I, q4(ex.gate), q4(ex.up), q4(ex.down))
-    return dev(inp.W_r.view(np.int16), torch.bfloat16), E
-
-
-def time_loop(torch, fn, steps, warmup):
-    for i in range(warmup):
-        fn(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(steps):
-        fn(warmup + i)
-    e1.record()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / 1e3
+    return moe.MoeLayer(_to_dev(torch, inp.W_r), E, None, inp.wl.k, inp.wl.T)
 
 
 def reduce_max(dist, v: float, device) -> float:
@@ -440,10 +545,13 @@ def job_value(world: int, tokens_per_step: int, steps: int, seconds: float) -> f
     return world * tokens_per_step * steps / seconds
 
 
+# ----------------------------------------------------------------------------- our arm
+
 def run_ours(args, rank, world):
     import torch
 
     import mixture_experts_layer_09_gb300 as moe
+    from mixture_experts_layer_09_gb300.run_case import upload
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -451,183 +559,185 @@ def run_ours(args, rank, world):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     moe.build()
-    H, I, E, k, T = WORKLOAD["H"], WORKLOAD["I"], WORKLOAD["E"], WORKLOAD["k"], WORKLOAD["T"]
+    P = HEADLINE
+    H, I, E, k, I_sh, T = P["H"], P["I"], P["E"], P["k"], P["I_sh"], P["T"]
     seed0 = rank_seed(rank)
+    hbm, tc, tc_sus, src = peaks()
 
-    # ---- resident weights: independent layer replicas
-    layers = []
-    for rep in range(N_REPLICAS):
-        ex = gen.draw_experts(seed0 + rep, E, H, I)
-        Wr = gen.draw_router(seed0 + rep, E, H)
-        inp = gen.LayerInputs(gen.Workload("b", T, H, I, E, k), None, None, Wr, ex, None)
-        W_r, Ed = upload_layer(torch, moe, inp)
-        layers.append(moe.MoeLayer(W_r, Ed, None, k, max_T=T))
-        del ex, inp
+    # ---- resident weights: independent layer replicas of the headline workload
+    layers = [upload(torch, moe, gen.Workload("p", T, H, I, E, k, I_sh=I_sh), seed0 + 50 + r)
+              for r in range(N_PREFILL_REPLICAS)]
+    xd = [_to_dev(torch, gen.draw_x(seed0 + 900 + i, T, H)) for i in range(N_PREFILL_INPUTS)]
+    rd = [_to_dev(torch, gen.draw_residual(seed0 + 950 + i, T, H)) for i in range(N_PREFILL_INPUTS)]
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
 
-    def inputs(Tb):
-        xs = [gen.draw_x(seed0 + 500 + i, Tb, H) for i in range(N_INPUTS)]
-        rs = [gen.draw_residual(seed0 + 700 + i, Tb, H) for i in range(N_INPUTS)]
-        to = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)  # noqa: E731
-        return [to(x).cuda() for x in xs], [to(r).cuda() for r in rs], [to(x).pin_memory() for x in xs], \
-            [to(r).pin_memory() for r in rs]
-
-    def measure(Tb, steps, warmup, full=False):
-        xd, rd, xh, rh = inputs(Tb)
-        y = torch.empty((Tb, H), dtype=torch.float32, device="cuda")
-        ids = torch.empty((Tb, k), dtype=torch.int32, device="cuda")
-
-        def step(i):
-            layers[i % N_REPLICAS].forward(xd[i % N_INPUTS], rd[i % N_INPUTS], y=y, topk_ids_out=ids)
-
-        out = {}
-        if dist is not None:
-            dist.barrier()
-        n0 = moe.moe_launch_count()
-        dt = time_loop(torch, step, steps, warmup)
-        out["launches_per_step"] = (moe.moe_launch_count() - n0) / (steps + warmup)
-        out["plain_s"] = reduce_max(dist, dt, "cuda")
-        # CUDA-graph replay of the same steps (one graph per (replica, input) pair)
-        graphs = []
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            step(0)
-        torch.cuda.current_stream().wait_stream(s)
-        torch.cuda.synchronize()
-        for i in range(N_INPUTS):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                step(i)
-            graphs.append(g)
-        dtg = time_loop(torch, lambda i: graphs[i % N_INPUTS].replay(), steps, warmup)
-        out["graph_s"] = reduce_max(dist, dtg, "cuda")
-        # distinct experts per step (routing is the GPU's own output)
-        nd = []
-        for i in range(N_INPUTS):
-            step(i)
-            torch.cuda.synchronize()
-            nd.append(len(np.unique(ids.cpu().numpy())))
-        out["n_distinct"] = nd
-        if full:
-            # per-kernel device time over a timed pass, CUDA events on the launching stream
-            moe.moe_profile_enable(True)
-            time_loop(torch, step, steps, 0)
-            out["kernels"] = moe.moe_profile_read()
-            moe.moe_profile_enable(False)
-            # end to end through host buffers: H2D of x and residual, D2H of y, every step
-            yh = torch.empty((Tb, H), dtype=torch.float32).pin_memory()
-            xin = torch.empty((Tb, H), dtype=torch.bfloat16, device="cuda")
-            rin = torch.empty((Tb, H), dtype=torch.bfloat16, device="cuda")
-
-            def e2e_step(i):
-                xin.copy_(xh[i % N_INPUTS], non_blocking=True)
-                rin.copy_(rh[i % N_INPUTS], non_blocking=True)
-                layers[i % N_REPLICAS].forward(xin, rin, y=y)
-                yh.copy_(y, non_blocking=True)
-
-            dte = time_loop(torch, e2e_step, steps, warmup)
-            out["e2e_s"] = reduce_max(dist, dte, "cuda")
-            out["h2d"] = 2 * Tb * H * 2
-            out["d2h"] = Tb * H * 4
-        return out
+    def step(i):
+        layers[i % N_PREFILL_REPLICAS].forward(xd[i % N_PREFILL_INPUTS], rd[i % N_PREFILL_INPUTS], y=y)
 
     # SM clocks are sampled (nvidia-smi, 200 ms) over the whole measurement phase, which
-    # contains the timed region: a region of a few ms alone would fall between two samples.
-    # the samples go to $BENCH_CLOCKS_DIR (default: the temporary directory)
+    # contains the timed region; the samples go to $BENCH_CLOCKS_DIR (default: the temp dir)
     clocks = Clocks(os.path.join(os.environ.get("BENCH_CLOCKS_DIR", tempfile.gettempdir()),
                                  f"clocks_bench_r{rank}.csv"), local)
     clocks.start()
-    main = measure(T, args.steps, args.warmup, full=True)
-    sweep = {}
-    for Tb in SWEEP_T:
-        r = measure(Tb, max(10, args.steps // 2), args.warmup)
-        best = min(r["plain_s"], r["graph_s"])
-        us = 1e6 * best / max(10, args.steps // 2)
-        sweep[f"T={Tb}"] = {"us_per_layer": us, "tokens_per_s": Tb / (us * 1e-6),
-                            "plain_us": 1e6 * r["plain_s"] / max(10, args.steps // 2),
-                            "graph_us": 1e6 * r["graph_s"] / max(10, args.steps // 2)}
+    n0 = moe.moe_launch_count()
+    total_s, per = timed_steps(torch, step, args.steps, args.warmup, dist)
+    launches = (moe.moe_launch_count() - n0) * args.steps / (args.steps + args.warmup)
+    head = summary(per)
+    perg = graph_steps(torch, step, N_PREFILL_INPUTS, args.steps, args.warmup)
+    graph = summary(perg)
+    kern = kernel_times(torch, moe, step, args.steps)
 
-    prefill = measure_prefill(torch, moe, args) if not args.no_prefill else None
+    # end to end through host buffers: H2D of x and the residual, the layer, D2H of y, every step
+    xh = [t.cpu().pin_memory() for t in xd]
+    rh = [t.cpu().pin_memory() for t in rd]
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    xin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    rin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+
+    def e2e_step(i):
+        xin.copy_(xh[i % N_PREFILL_INPUTS], non_blocking=True)
+        rin.copy_(rh[i % N_PREFILL_INPUTS], non_blocking=True)
+        layers[i % N_PREFILL_REPLICAS].forward(xin, rin, y=y)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_s, _ = timed_steps(torch, e2e_step, args.steps, args.warmup, dist)
+    del layers, xd, rd
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads (reported beside the headline)
     extra = {}
     if not args.no_extra:
-        extra = {"decode_with_rmsnorm": measure_norm(torch, moe, args, layers, T, H),
-                 "decode_glm": measure_glm(torch, moe, args),
-                 "router_dispatch_sweep": measure_router_sweep(torch, moe, args),
-                 "skewed_layer": measure_skewed_layer(torch, moe, args),
-                 "mxfp4": measure_mxfp4(torch, moe, args)}
-    main["clocks"] = clocks.stop()
+        extra["decode"] = measure_decode(torch, moe, args, seed0)
+        extra["decode_glm"] = measure_glm(torch, moe, args)
+        extra["prefill_t512"] = measure_prefill_t512(torch, moe, args, seed0)
+        extra["decode_with_rmsnorm"] = measure_norm(torch, moe, args, seed0)
+        extra["router_dispatch_sweep"] = measure_router_sweep(torch, moe, args)
+        extra["skewed_layer"] = measure_skewed_layer(torch, moe, args)
+        extra["mxfp4"] = measure_mxfp4(torch, moe, args)
+    clk = clocks.stop()
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
         return
-    steps = args.steps
-    best_s = min(main["plain_s"], main["graph_s"])
-    ms_step = 1e3 * best_s / steps
-    value = job_value(world, T, steps, best_s)
-    hbm, tc, src = peaks()
-    # roofline of the dominant kernel (by device time)
-    kern = main["kernels"]
+
+    fl = prefill_flops(T, H, I, E, k, I_sh)
+    ms_step = 1e3 * total_s / args.steps
+    value = job_value(world, T, args.steps, total_s)
     dom = max(kern, key=lambda n: kern[n][0])
-    dom_ms = kern[dom][0] / max(kern[dom][1], 1)
-    nd = float(np.mean(main["n_distinct"]))
-    bpe = BYTES_PER_EXPERT(H, I)
-    per_kernel_bytes = {
-        "gateup_gemv": nd * (2 * I * H // 2 + 2 * I * (H // 32) * 2) + T * H * 2 + T * (H // 32) * 8 + T * k * I * 4,
-        "down_gemv_combine": nd * (H * I // 2 + H * (I // 32) * 2) + T * k * I * 2 + T * k * (I // 32) * 8
-        + T * H * 2 + T * H * 4,
-    }
-    ach = per_kernel_bytes.get(dom, float("nan")) / (dom_ms * 1e-3) / 1e9
-    traffic = dram_traffic(dom, nd)
-    layer_bytes = nd * bpe + E * H * 2 + T * H * (2 + 2 + 4)
-    layer_gbs = layer_bytes / (ms_step * 1e-3) / 1e9
+    dom_us = 1e3 * kern[dom][0] / max(kern[dom][1], 1)
+    if dom in ("gemm_gateup", "gemm_down"):
+        ach = fl[dom] / (dom_us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tc, "unit": "TFLOP/s", "frac": ach / tc,
+                "peak_source": f"bf16 dense burst, {src} (the MMAs take fp16 operands, same dense rate)",
+                "algorithmic_flops": fl[dom], "kernel_us": dom_us}
+    else:
+        roof = {"bound": "tensor", "kernel": dom, "achieved": None, "peak": tc, "unit": "TFLOP/s", "frac": None,
+                "kernel_us": dom_us, "note": "dominant kernel is not a GEMM"}
+    tr = dram_traffic(dom)
+    roof["traffic"] = tr["bytes"] if tr else None
+    roof["traffic_note"] = tr["note"] if tr else "no ncu capture of this kernel's current source"
+    kus = {n: 1e3 * v[0] / max(v[1], 1) for n, v in kern.items()}
+    cfg = {"workload": f"{P['name']} H={H} I={I} E={E} k={k} I_sh={I_sh} T={T}", "global_batch": T * world,
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+           "l2": f"{N_PREFILL_REPLICAS} layer replicas x {(E * BYTES_PER_EXPERT(H, I) + BYTES_PER_EXPERT(H, I_sh)) / 1e6:.0f}"
+                 f" MB of experts cycled with {N_PREFILL_INPUTS} distinct batches (inputs larger than L2)",
+           "us_per_layer": ms_step * 1e3, "median_us": head["median_us"], "p10_us": head["p10_us"],
+           "p90_us": head["p90_us"], "graph_median_us": graph["median_us"],
+           "layer_tflops": fl["layer"] / (head["median_us"] * 1e-6) / 1e12,
+           "layer_tc_frac": fl["layer"] / (head["median_us"] * 1e-6) / 1e12 / tc}
+    for name in ("gemm_gateup", "gemm_down"):
+        if name in kus:
+            cfg[f"{name}_us"] = kus[name]
+            cfg[f"{name}_tc_frac"] = fl[name] / (kus[name] * 1e-6) / 1e12 / tc
+    for name, v in kus.items():
+        cfg[f"kernel_us.{name}"] = v
+    # flat copies of the other workloads' figures, so that they stay with the line's record
+    if "decode" in extra:
+        for Tb, d in extra["decode"].items():
+            tag = f"decode_qwen3_{Tb.replace('=', '').lower()}"
+            cfg[f"{tag}_us"] = d["us_per_layer"]
+            cfg[f"{tag}_tok_s"] = d["tokens_per_s"]
+            cfg[f"{tag}_hbm_frac"] = d["hbm_frac"]
+            for kn, kv in d.get("kernels", {}).items():
+                cfg[f"{tag}_{kn}_hbm_frac"] = kv["hbm_frac"]
+    if "decode_glm" in extra:
+        for key, d in extra["decode_glm"].items():
+            if isinstance(d, dict):
+                tag = "decode_glm_" + key.replace("=", "").replace(",", "_").lower()
+                cfg[f"{tag}_us"] = d["us_per_layer"]
+                cfg[f"{tag}_tok_s"] = d["tokens_per_s"]
+                cfg[f"{tag}_hbm_frac"] = d["hbm_frac"]
+    if "prefill_t512" in extra:
+        d = extra["prefill_t512"]
+        for key in ("us_per_layer", "tokens_per_s", "layer_tc_frac", "roof_frac"):
+            cfg[f"prefill_t512_{key}"] = d[key]
+    if "skewed_layer" in extra:
+        cfg["skewed_t8192_us"] = extra["skewed_layer"]["us_per_layer"]
+    if "router_dispatch_sweep" in extra:
+        d = extra["router_dispatch_sweep"].get("E=256,T=16384")
+        if d:
+            cfg["router_dispatch_e256_t16384_us"] = d["us"]
+
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int4xbf16->fp32", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD['name']} H={H} I={I} E={E} k={k} T={T}", "global_batch": T * world,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": f"{N_REPLICAS} layer replicas x {E * bpe / 1e6:.0f} MB of experts cycled with "
-                         f"{N_INPUTS} distinct batches (inputs larger than L2)",
-                   "us_per_layer": ms_step * 1e3,
-                   "plain_us_per_layer": 1e6 * main["plain_s"] / steps,
-                   "graph_us_per_layer": 1e6 * main["graph_s"] / steps,
-                   "mean_distinct_experts": nd,
-                   "layer_hbm_gbs": layer_gbs, "layer_hbm_frac": layer_gbs / hbm,
-                   "sweep": sweep},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                     "frac": ach / hbm, "peak_source": src,
-                     "traffic": traffic["bytes"] if traffic else None,
-                     "traffic_note": traffic["note"] if traffic else "no ncu capture of this kernel's current source",
-                     "algorithmic_bytes": per_kernel_bytes.get(dom), "kernel_us": dom_ms * 1e3},
-        "kernels_us_per_step": {n: 1e3 * v[0] / steps for n, v in kern.items()},
-        "gpu_launches": int(round(main["launches_per_step"] * steps)),
-        "prefill": prefill,
+        "config": cfg,
+        "roofline": roof,
+        "gpu_launches": int(round(launches)),
+        "clocks": clk,
+        "e2e": {"value": job_value(world, T, args.steps, e2e_s), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": T * H * 4},
         **extra,
-        "clocks": main.get("clocks"),
-        "e2e": {"value": job_value(world, T, steps, main["e2e_s"]), "unit": "tokens/s",
-                "h2d_bytes_per_step": main["h2d"], "d2h_bytes_per_step": main["d2h"]},
     }
     if not args.no_cpu_baseline:
-        # the oracle as it stands, one host thread, on whole batches of the same workload (one
-        # drawn layer, a fresh token batch each time) until about 10 s of CPU work is done
-        import dataclasses
-
         import oracle
-        oracle.build()
-        base = gen.draw_layer(gen.Workload(WORKLOAD["name"], T, H, I, E, k))
-        n_tok, dt, b = 0, 0.0, 0
-        while b == 0 or dt < 10.0:
-            inp = dataclasses.replace(base, x=gen.draw_x(500 + b, T, H)) if b else base
-            t0 = time.perf_counter()
-            oracle.layer_forward(inp)
-            dt += time.perf_counter() - t0
-            n_tok += T
-            b += 1
-        line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": f"{b} batches of T={T} tokens ({n_tok} tokens, {dt:.1f} s)"}
+        cores = oracle.default_threads()
+        v, n_tok, dt, thr, nb = oracle_slices(16, args.cpu_seconds, cores)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{nb} batches of 16 tokens of the headline shape ({n_tok} tokens, "
+                                          f"{dt:.1f} s) on {thr} threads"}
+        v1, n1, dt1, thr1, nb1 = oracle_slices(4, args.cpu_seconds, 1)
+        line["cpu_baseline_single_thread"] = {"value": v1, "unit": "tokens/s", "cores": thr1, "kind": "oracle",
+                                              "sample": f"{nb1} batches of 4 tokens ({n1} tokens, {dt1:.1f} s)"}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def measure_prefill_t512(torch, moe, args, seed0):
+    """The prefill layer at T=512: about 34 rows per routed expert, so its roof is
+    max(bytes / HBM, FLOPs / tensor peak); both fractions and that roof's are reported."""
+    from mixture_experts_layer_09_gb300.run_case import upload
+    P = HEADLINE
+    H, I, E, k, I_sh, T = P["H"], P["I"], P["E"], P["k"], P["I_sh"], 512
+    hbm, tc, _, _ = peaks()
+    layers = [upload(torch, moe, gen.Workload("p5", T, H, I, E, k, I_sh=I_sh), seed0 + 60 + r)
+              for r in range(N_PREFILL_REPLICAS)]
+    xs = [_to_dev(torch, gen.draw_x(seed0 + 1100 + i, T, H)) for i in range(N_PREFILL_INPUTS)]
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+
+    def step(i):
+        layers[i % N_PREFILL_REPLICAS].forward(xs[i % N_PREFILL_INPUTS], None, y=y, topk_ids_out=ids)
+
+    _, per = timed_steps(torch, step, max(50, args.steps), args.warmup)
+    nd = []
+    for i in range(N_PREFILL_INPUTS):
+        step(i)
+        nd.append(int(torch.unique(ids).numel()))
+    kern = kernel_times(torch, moe, step, max(20, args.steps // 2))
+    del layers
+    torch.cuda.empty_cache()
+    us = summary(per)["median_us"]
+    fl = prefill_flops(T, H, I, E, k, I_sh)
+    byts = float(np.mean(nd)) * BYTES_PER_EXPERT(H, I) + BYTES_PER_EXPERT(H, I_sh) + E * H * 2 + T * H * (2 + 2 + 4)
+    roof_us = max(byts / (hbm * 1e9), fl["layer"] / (tc * 1e12)) * 1e6
+    n = max(20, args.steps // 2)
+    return {"us_per_layer": us, "tokens_per_s": T / (us * 1e-6),
+            "layer_tc_frac": fl["layer"] / (us * 1e-6) / 1e12 / tc,
+            "layer_hbm_frac": byts / (us * 1e-6) / 1e9 / hbm, "roof_us": roof_us, "roof_frac": roof_us / us,
+            "kernels_us": {nm: 1e3 * v[0] / n for nm, v in kern.items()}}
 
 
 def main():
@@ -637,9 +747,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-prefill", action="store_true", help="skip the prefill-layer section")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU time of each oracle timing")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the GLM-class decode, router/dispatch sweep and skewed-layer sections")
+                    help="skip the decode, GLM-class, T=512, router/dispatch sweep, skewed and MXFP4 sections")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

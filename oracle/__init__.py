@@ -5,7 +5,9 @@ and the benchmark's CPU-baseline / reference leg import this package.  The CUDA
 library never calls it and shares no code with it.
 
 ``build()`` compiles moe_oracle.c with gcc into ``oracle/libmoe_oracle.so``
-(in-tree, git-ignored).  The functions below take numpy arrays (bf16/fp16 as
+(in-tree, git-ignored).  Independent rows run on every available host core by
+default (``set_threads``); the per-row arithmetic is the same sequential loop
+for any thread count.  The functions below take numpy arrays (bf16/fp16 as
 uint16 bit patterns) and return numpy arrays.
 """
 from __future__ import annotations
@@ -28,7 +30,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(
             os.path.getmtime(SRC), os.path.getmtime(os.path.join(HERE, "moe_oracle.h"))):
         tmp = LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, SRC, "-lm"])
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-pthread", "-fPIC", "-shared", "-o", tmp, SRC, "-lm"])
         os.replace(tmp, LIB)
     return LIB
 
@@ -46,7 +48,25 @@ def lib():
         _lib.mo_e2m1_to_f64.argtypes = [C.c_int]
         _lib.mo_ue8m0_to_f64.restype = C.c_double
         _lib.mo_ue8m0_to_f64.argtypes = [C.c_uint8]
+        _lib.mo_set_threads(default_threads())
     return _lib
+
+
+def default_threads() -> int:
+    """Worker threads of the oracle: the host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def set_threads(n: int) -> None:
+    """Worker threads for independent rows; results are bit-identical for any count."""
+    lib().mo_set_threads(int(n))
+
+
+def get_threads() -> int:
+    return int(lib().mo_get_threads())
 
 
 def _p(a: Optional[np.ndarray]):

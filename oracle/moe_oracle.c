@@ -3,18 +3,73 @@
  *
  * TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT (see moe_oracle.h).  Written for
  * a reader checking it against the pages by eye: one loop per definition, fp64
- * throughout, no blocking, fusion or reordering.  Single-threaded.
+ * throughout, no blocking, fusion or reordering.  Independent rows (router
+ * logits per token, expert rows, shared-expert tokens) may be spread over
+ * worker threads (mo_set_threads); each row is still computed by the same
+ * sequential loop, so the results do not depend on the thread count.
  *
  * Parity pins (tests/test_oracle_pins.py): brute-force full sort for top-k,
  * hand-decoded nibbles (int4 and MXFP4), closed forms of the MLP, the MXFP4 MLP against
  * its exact int4 twin, dispatch invariants, the
  * zero-weight invariance of the combine, and tests/golden fixtures.
  */
+#define _POSIX_C_SOURCE 200809L
 #include "moe_oracle.h"
 
 #include <math.h>
+#include <pthread.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* ---- worker threads over independent rows (no arithmetic here) */
+#define MO_MAX_THREADS 256
+static int g_threads = 1;
+
+void mo_set_threads(int n) { g_threads = n < 1 ? 1 : (n > MO_MAX_THREADS ? MO_MAX_THREADS : n); }
+int mo_get_threads(void) { return g_threads; }
+
+typedef int (*mo_row_fn)(void* ctx, long i);
+struct mo_job {
+    mo_row_fn fn;
+    void* ctx;
+    long n;
+    int nthr, tid, rc;
+};
+
+/* Thread tid takes rows tid, tid + nthr, ... and stops at its first error. */
+static void* mo_worker(void* arg) {
+    struct mo_job* j = (struct mo_job*)arg;
+    for (long i = j->tid; i < j->n; i += j->nthr) {
+        int rc = j->fn(j->ctx, i);
+        if (rc) {
+            j->rc = rc;
+            break;
+        }
+    }
+    return NULL;
+}
+
+/* Runs fn(ctx, i) for i = 0 .. n-1; returns the first non-zero code in thread order. */
+static int mo_for_rows(long n, mo_row_fn fn, void* ctx) {
+    int nthr = g_threads;
+    if (n < nthr) nthr = (int)(n > 0 ? n : 1);
+    struct mo_job jobs[MO_MAX_THREADS];
+    pthread_t th[MO_MAX_THREADS];
+    int started[MO_MAX_THREADS];
+    for (int t = 0; t < nthr; ++t) {
+        jobs[t].fn = fn; jobs[t].ctx = ctx; jobs[t].n = n;
+        jobs[t].nthr = nthr; jobs[t].tid = t; jobs[t].rc = 0;
+        started[t] = t > 0 && pthread_create(&th[t], NULL, mo_worker, &jobs[t]) == 0;
+    }
+    for (int t = 0; t < nthr; ++t)
+        if (!started[t]) mo_worker(&jobs[t]);  /* thread 0, or a thread that could not start */
+    int rc = 0;
+    for (int t = 0; t < nthr; ++t) {
+        if (started[t]) pthread_join(th[t], NULL);
+        if (!rc) rc = jobs[t].rc;
+    }
+    return rc;
+}
 
 /* bf16 is the top half of an IEEE binary32; widening is exact. */
 double mo_bf16_to_f64(uint16_t bits) {
@@ -39,13 +94,21 @@ double mo_f16_to_f64(uint16_t bits) {
     return sign ? -v : v;
 }
 
+/* Every fp16 bit pattern decoded once by mo_f16_to_f64, when the library is
+ * loaded (a lookup instead of a per-weight ldexp; the values are the same). */
+static double g_f16_table[65536];
+__attribute__((constructor)) static void fill_f16_table(void) {
+    for (int b = 0; b < 65536; ++b) g_f16_table[b] = mo_f16_to_f64((uint16_t)b);
+}
+static double f16_value(uint16_t bits) { return g_f16_table[bits]; }
+
 /* One weight element of an int4 matrix (colibri #418, "Correctness": int4 is
  * offset-binary, value = nibble - 8, in the CPU byte layout; "Grouped scales in
  * the Vulkan kernels": one scale per group of K-columns, here 32). */
 static double weight_at(const uint8_t* q, const uint16_t* s, int K, int n, int c) {
     uint8_t byte = q[(size_t)n * (K / 2) + c / 2];
     int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
-    return (double)(nib - 8) * mo_f16_to_f64(s[(size_t)n * (K / 32) + c / 32]);
+    return (double)(nib - 8) * f16_value(s[(size_t)n * (K / 32) + c / 32]);
 }
 
 int mo_dequant(const uint8_t* q, const uint16_t* s, int rows, int K, double* w) {
@@ -104,25 +167,35 @@ static size_t scale_bytes(int fmt) { return fmt == MO_FMT_MXFP4 ? 1 : 2; }
 /* Router logits: one GEMV row per expert over the hidden row, and the shared
  * expert's gate logit as one more row "past the router's logits"
  * (dasLLAMA #3988, decode span and routed-block commits). */
+struct logits_ctx {
+    const uint16_t *x, *W_r, *g;
+    int H, E;
+    double* logits;
+};
+
+static int logits_token(void* vc, long t) {
+    const struct logits_ctx* c = (const struct logits_ctx*)vc;
+    int H = c->H, E = c->E, ld = E + (c->g ? 1 : 0);
+    for (int e = 0; e < E; ++e) {
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h)
+            acc += mo_bf16_to_f64(c->x[(size_t)t * H + h]) * mo_bf16_to_f64(c->W_r[(size_t)e * H + h]);
+        c->logits[(size_t)t * ld + e] = acc;
+    }
+    if (c->g) {
+        double acc = 0.0;
+        for (int h = 0; h < H; ++h)
+            acc += mo_bf16_to_f64(c->x[(size_t)t * H + h]) * mo_bf16_to_f64(c->g[h]);
+        c->logits[(size_t)t * ld + E] = acc;
+    }
+    return 0;
+}
+
 int mo_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g,
                      int T, int H, int E, double* logits) {
     if (!x || !W_r || !logits || T < 0 || H <= 0 || E <= 0) return -1;
-    int ld = E + (g ? 1 : 0);
-    for (int t = 0; t < T; ++t) {
-        for (int e = 0; e < E; ++e) {
-            double acc = 0.0;
-            for (int h = 0; h < H; ++h)
-                acc += mo_bf16_to_f64(x[(size_t)t * H + h]) * mo_bf16_to_f64(W_r[(size_t)e * H + h]);
-            logits[(size_t)t * ld + e] = acc;
-        }
-        if (g) {
-            double acc = 0.0;
-            for (int h = 0; h < H; ++h)
-                acc += mo_bf16_to_f64(x[(size_t)t * H + h]) * mo_bf16_to_f64(g[h]);
-            logits[(size_t)t * ld + E] = acc;
-        }
-    }
-    return 0;
+    struct logits_ctx c = {x, W_r, g, H, E, logits};
+    return mo_for_rows(T, logits_token, &c);
 }
 
 /* Softmax top-k router (vllm.cpp #481, warp-router commit: softmax over the
@@ -287,6 +360,30 @@ int mo_expert_row(const uint16_t* x_row, int H, int I,
     return mo_expert_row_fmt(x_row, H, I, MO_FMT_INT4, gq, gs, uq, us, dq, ds, o);
 }
 
+struct mlp_ctx {
+    const uint16_t* x;
+    int H, I, E, k, fmt;
+    const uint8_t *gate_q, *up_q, *down_q;
+    const uint8_t *gs, *us, *ds;  /* scale arrays walked in bytes */
+    size_t gq_sz, gs_sz, dq_sz, ds_sz;
+    const int32_t *ids, *perm;
+    const uint8_t* token_mask;
+    double* rows;
+};
+
+/* Dispatched row r: a = perm[r], t = a / k, e = ids[a]; rows[r] = expert e on x[t]. */
+static int mlp_row(void* vc, long r) {
+    const struct mlp_ctx* c = (const struct mlp_ctx*)vc;
+    int a = c->perm[r], t = a / c->k, e = c->ids[a];
+    if (e < 0 || e >= c->E) return -1;
+    if (c->token_mask && !c->token_mask[t]) return 0;
+    return mo_expert_row_fmt(c->x + (size_t)t * c->H, c->H, c->I, c->fmt,
+                             c->gate_q + e * c->gq_sz, c->gs + e * c->gs_sz,
+                             c->up_q + e * c->gq_sz, c->us + e * c->gs_sz,
+                             c->down_q + e * c->dq_sz, c->ds + e * c->ds_sz,
+                             c->rows + (size_t)r * c->H);
+}
+
 int mo_expert_mlp_fmt(const uint16_t* x, int T, int H, int I, int E, int k, int fmt,
                       const uint8_t* gate_q, const void* gate_s,
                       const uint8_t* up_q, const void* up_s,
@@ -295,23 +392,14 @@ int mo_expert_mlp_fmt(const uint16_t* x, int T, int H, int I, int E, int k, int 
                       const uint8_t* token_mask, double* rows) {
     if (!x || !ids || !perm || !rows || T < 0 || E <= 0 || k < 1) return -1;
     if (!gate_s || !up_s || !down_s) return -1;
-    size_t gq_sz = (size_t)I * (H / 2), gs_sz = (size_t)I * (H / 32) * scale_bytes(fmt);
-    size_t dq_sz = (size_t)H * (I / 2), ds_sz = (size_t)H * (I / 32) * scale_bytes(fmt);
-    const uint8_t* gs = (const uint8_t*)gate_s;  /* scale arrays walked in bytes */
-    const uint8_t* us = (const uint8_t*)up_s;
-    const uint8_t* ds = (const uint8_t*)down_s;
-    for (int r = 0; r < T * k; ++r) {
-        int a = perm[r], t = a / k, e = ids[a];
-        if (e < 0 || e >= E) return -1;
-        if (token_mask && !token_mask[t]) continue;
-        int rc = mo_expert_row_fmt(x + (size_t)t * H, H, I, fmt,
-                                   gate_q + e * gq_sz, gs + e * gs_sz,
-                                   up_q + e * gq_sz, us + e * gs_sz,
-                                   down_q + e * dq_sz, ds + e * ds_sz,
-                                   rows + (size_t)r * H);
-        if (rc) return rc;
-    }
-    return 0;
+    struct mlp_ctx c;
+    c.x = x; c.H = H; c.I = I; c.E = E; c.k = k; c.fmt = fmt;
+    c.gate_q = gate_q; c.up_q = up_q; c.down_q = down_q;
+    c.gs = (const uint8_t*)gate_s; c.us = (const uint8_t*)up_s; c.ds = (const uint8_t*)down_s;
+    c.gq_sz = (size_t)I * (H / 2); c.gs_sz = (size_t)I * (H / 32) * scale_bytes(fmt);
+    c.dq_sz = (size_t)H * (I / 2); c.ds_sz = (size_t)H * (I / 32) * scale_bytes(fmt);
+    c.ids = ids; c.perm = perm; c.token_mask = token_mask; c.rows = rows;
+    return mo_for_rows((long)T * k, mlp_row, &c);
 }
 
 int mo_expert_mlp(const uint16_t* x, int T, int H, int I, int E, int k,
@@ -326,27 +414,43 @@ int mo_expert_mlp(const uint16_t* x, int T, int H, int I, int E, int k,
 
 /* Shared expert scaled by sigmoid of its gate logit; an ungated shared expert
  * adds at weight one (dasLLAMA #3988, decode span commit). */
+struct shared_ctx {
+    const uint16_t* x;
+    int H, I_sh, fmt;
+    const uint8_t *gate_q, *up_q, *down_q;
+    const void *gate_s, *up_s, *down_s;
+    const uint16_t* g;
+    const uint8_t* token_mask;
+    double* y_sh;
+};
+
+static int shared_token(void* vc, long t) {
+    const struct shared_ctx* c = (const struct shared_ctx*)vc;
+    int H = c->H;
+    if (c->token_mask && !c->token_mask[t]) return 0;
+    const uint16_t* xr = c->x + (size_t)t * H;
+    int rc = mo_expert_row_fmt(xr, H, c->I_sh, c->fmt, c->gate_q, c->gate_s, c->up_q, c->up_s,
+                               c->down_q, c->down_s, c->y_sh + (size_t)t * H);
+    if (rc) return rc;
+    double gate = 1.0;
+    if (c->g) {
+        double z = 0.0;
+        for (int h = 0; h < H; ++h) z += mo_bf16_to_f64(xr[h]) * mo_bf16_to_f64(c->g[h]);
+        gate = 1.0 / (1.0 + exp(-z));
+    }
+    for (int n = 0; n < H; ++n) c->y_sh[(size_t)t * H + n] *= gate;
+    return 0;
+}
+
 int mo_shared_expert_fmt(const uint16_t* x, int T, int H, int I_sh, int fmt,
                          const uint8_t* gate_q, const void* gate_s,
                          const uint8_t* up_q, const void* up_s,
                          const uint8_t* down_q, const void* down_s,
                          const uint16_t* g, const uint8_t* token_mask, double* y_sh) {
     if (!x || !y_sh || T < 0) return -1;
-    for (int t = 0; t < T; ++t) {
-        if (token_mask && !token_mask[t]) continue;
-        const uint16_t* xr = x + (size_t)t * H;
-        int rc = mo_expert_row_fmt(xr, H, I_sh, fmt, gate_q, gate_s, up_q, up_s, down_q, down_s,
-                                   y_sh + (size_t)t * H);
-        if (rc) return rc;
-        double gate = 1.0;
-        if (g) {
-            double z = 0.0;
-            for (int h = 0; h < H; ++h) z += mo_bf16_to_f64(xr[h]) * mo_bf16_to_f64(g[h]);
-            gate = 1.0 / (1.0 + exp(-z));
-        }
-        for (int n = 0; n < H; ++n) y_sh[(size_t)t * H + n] *= gate;
-    }
-    return 0;
+    struct shared_ctx c = {x, H, I_sh, fmt, gate_q, up_q, down_q, gate_s, up_s, down_s,
+                           g, token_mask, y_sh};
+    return mo_for_rows(T, shared_token, &c);
 }
 
 int mo_shared_expert(const uint16_t* x, int T, int H, int I_sh,

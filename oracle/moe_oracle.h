@@ -35,6 +35,12 @@ extern "C" {
 double mo_bf16_to_f64(uint16_t bits);
 double mo_f16_to_f64(uint16_t bits);
 
+/* Worker threads for independent rows (router logits per token, dispatched
+ * expert rows, shared-expert tokens); default 1.  Every row is computed by the
+ * same sequential loop whatever the count, so results are bit-identical. */
+void mo_set_threads(int n);
+int mo_get_threads(void);
+
 /* Dequantise rows x K of one int4 matrix into w[rows][K] (fp64). */
 int mo_dequant(const uint8_t* q, const uint16_t* s, int rows, int K, double* w);
 

@@ -1,7 +1,9 @@
 """GPU parity of the expert MLP (both arms), the combine and the whole layer against the fp64
 oracle, on the workloads' shapes.  Routing (ids) is bit-exact; float outputs meet rel-L2 <= 1e-3
-and max-abs <= 2e-3 * max|ref|.  Large workloads are checked on sampled tokens, which the oracle
-computes one by one; routing is compared for every token."""
+and max-abs <= 2e-3 * max|ref|.  Every element is compared up to the T=512 prefill layer and
+the GLM-class T=8 layers; at T=4096 the compared tokens cover every token tile of every expert
+bucket at several rows (the oracle computes them one by one); routing is compared for every
+token."""
 import numpy as np
 import pytest
 
@@ -82,13 +84,18 @@ def _layer_gpu(moe, inp, arm=0):
 
 
 def _check_layer(moe, inp, arm=0, sample=None):
+    """sample=None: every token; "buckets": wk.bucket_sample_tokens; an int n: tokens 0, T-1
+    and n random others."""
     T = inp.wl.T
     if sample is None:
         mask = None
         toks = np.arange(T)
     else:
-        g = gen.rng(99, T)
-        toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(sample, T), replace=False)]))
+        if sample == "buckets":
+            toks = wk.bucket_sample_tokens(inp)
+        else:
+            g = gen.rng(99, T)
+            toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(sample, T), replace=False)]))
         mask = np.zeros(T, dtype=np.uint8)
         mask[toks] = 1
     ref = oracle.layer_forward(inp, token_mask=mask)
@@ -117,15 +124,39 @@ def test_layer_qwen3_decode(moe, name):
     _check_layer(moe, wk.layer(name))
 
 
-@pytest.mark.parametrize("name,sample", [("glm_decode_k8_t1", None), ("glm_decode_k8_t8", 3),
-                                         ("glm_decode_k32_t1", None), ("glm_decode_k32_t8", 2)])
-def test_layer_glm_decode(moe, name, sample):
-    _check_layer(moe, wk.layer(name), sample=sample)
+@pytest.mark.parametrize("name", ["glm_decode_k8_t1", "glm_decode_k8_t8", "glm_decode_k32_t1", "glm_decode_k32_t8"])
+def test_layer_glm_decode(moe, name):
+    _check_layer(moe, wk.layer(name))
 
 
-@pytest.mark.parametrize("name,sample", [("qwen15_prefill_t512", 6), ("qwen15_prefill_t4096", 6)])
-def test_layer_qwen15_prefill(moe, name, sample):
-    _check_layer(moe, wk.layer(name), sample=sample)
+@pytest.mark.parametrize("arm", [0, 1])
+def test_layer_qwen15_prefill_t512_every_element(moe, arm):
+    """The full T=512 prefill layer with its gated shared expert, every element of y: all 11
+    gate/up and 16 down row blocks of the routed experts, all 44 gate/up row blocks of the
+    shared expert, on the arm the library picks (the tensor arm) and on the bandwidth arm."""
+    _check_layer(moe, wk.layer("qwen15_prefill_t512"), arm=arm)
+
+
+def test_layer_qwen15_prefill_t4096(moe):
+    _check_layer(moe, wk.layer("qwen15_prefill_t4096"), sample="buckets")
+
+
+@pytest.mark.parametrize("arm", [2, 1])
+def test_expert_mlp_rows_qwen15_t512_every_row(moe, arm):
+    """moe_expert_mlp at the full prefill shape (H=2048, I=1408, E=60, k=4, T=512): all 2,048
+    dispatched rows, every element, unweighted in dispatch order."""
+    import torch
+    inp = wk.layer("qwen15_prefill_t512", I_sh=0, seed=3)
+    wl = inp.wl
+    ids, w, (counts, offsets, perm, inv) = _routing(inp)
+    ref = oracle.expert_mlp(inp.x, inp.experts, ids, perm)
+    x, r, W_r, E, S = wk.upload(inp)
+    rows = wk.poison(torch.empty((wl.T * wl.k, wl.H), dtype=torch.float32, device="cuda"))
+    ws = torch.zeros(moe.moe_expert_mlp_workspace_size(wl.T, wl.k, wl.E, wl.H, wl.I), dtype=torch.uint8,
+                     device="cuda")
+    moe.moe_expert_mlp(x, wl.k, E, wk.dev(offsets), wk.dev(perm), rows, ws, arm=arm)
+    assert moe.moe_device_status(ws) == 0
+    wk.assert_close(rows.cpu().numpy(), ref, f"rows arm={arm}")
 
 
 @pytest.mark.parametrize("arm", [1, 2])
@@ -138,8 +169,8 @@ def test_layer_tiny_zipf_t8192(moe, arm):
 def test_layer_qwen15_prefill_gemv_arm_agrees(moe):
     """Both arms on the same prefill batch: each within tolerance of the oracle."""
     inp = wk.layer("qwen15_prefill_t512", T=96)
-    _check_layer(moe, inp, arm=1, sample=4)
-    _check_layer(moe, inp, arm=2, sample=4)
+    _check_layer(moe, inp, arm=1)
+    _check_layer(moe, inp, arm=2)
 
 
 def _bf16_ulp_distance(a_bits, b_bits):

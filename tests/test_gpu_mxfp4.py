@@ -85,8 +85,7 @@ def _check_layer(moe, inp, arm=0, sample=None):
     if sample is None:
         mask, toks = None, np.arange(T)
     else:
-        g = gen.rng(98, T)
-        toks = np.unique(np.concatenate([[0, T - 1], g.choice(T, size=min(sample, T), replace=False)]))
+        toks = wk.bucket_sample_tokens(inp)
         mask = np.zeros(T, dtype=np.uint8)
         mask[toks] = 1
     ref = oracle.layer_forward(inp, token_mask=mask)
@@ -116,4 +115,4 @@ def test_layer_qwen3_decode_t16_mxfp4(moe):
 
 
 def test_layer_qwen15_prefill_t4096_mxfp4(moe):
-    _check_layer(moe, wk.layer("qwen15_prefill_t4096_mxfp4"), sample=6)
+    _check_layer(moe, wk.layer("qwen15_prefill_t4096_mxfp4"), sample="buckets")

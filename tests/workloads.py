@@ -62,6 +62,26 @@ def layer(name: str, seed: int = 0, **over) -> gen.LayerInputs:
     return enforce_margin_x(gen.draw_layer(wl))
 
 
+def bucket_sample_tokens(inp: gen.LayerInputs, stride: int = 64) -> np.ndarray:
+    """Tokens to compare on a layer too large for the oracle to finish whole: every expert
+    bucket (from the oracle's own routing of all tokens) contributes its first and last
+    dispatched row and every `stride`-th row between, and the tokens of those rows are taken.
+    Buckets are cut into token tiles of at most 256 rows, so every tile of every expert holds
+    sampled rows at several positions; the tokens fall across the whole batch, so every tile
+    of the shared expert is sampled too."""
+    wl = inp.wl
+    logits = oracle.router_logits(inp.x, inp.W_r).astype(np.float32).astype(np.float64)
+    ids, _ = oracle.router_topk(logits, wl.k)
+    _, offsets, perm, _ = oracle.dispatch(ids, wl.E)
+    rows = []
+    for e in range(wl.E):
+        b0, b1 = int(offsets[e]), int(offsets[e + 1])
+        if b1 > b0:
+            rows.extend(range(b0, b1, stride))
+            rows.append(b1 - 1)
+    return np.unique(perm[np.asarray(rows, dtype=np.int64)] // wl.k)
+
+
 def rel_errors(got, ref):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
