@@ -89,7 +89,8 @@ enum {
 };
 
 enum {
-    MOE_ARM_AUTO = 0,  /* GEMV when T <= MOE_AUTO_GEMV_MAX_T, grouped GEMM otherwise */
+    MOE_ARM_AUTO = 0,  /* GEMV while T * k <= MOE_AUTO_GEMV_ROWS_PER_EXPERT * E and, with a shared
+                          expert, T <= MOE_AUTO_GEMV_MAX_T_SHARED; grouped GEMM otherwise */
     MOE_ARM_GEMV = 1,  /* bandwidth arm: fused int4 GEMV, weights streamed once per call */
     MOE_ARM_GEMM = 2   /* tensor arm: grouped GEMM on tcgen05 / TMEM */
 };
@@ -97,7 +98,11 @@ enum {
 /* Size limits checked on the host. */
 #define MOE_MAX_E 256
 #define MOE_MAX_K 32
-#define MOE_AUTO_GEMV_MAX_T 32
+/* Arm choice of MOE_ARM_AUTO, from a sweep of both arms over T on one GB300 (the GEMV arm
+ * streams each routed expert's weights once per pass of up to 4 of its tokens, and the shared
+ * expert's once per 4 tokens of the batch; the GEMM arm costs a latency floor of ~200 us). */
+#define MOE_AUTO_GEMV_ROWS_PER_EXPERT 4
+#define MOE_AUTO_GEMV_MAX_T_SHARED 16
 #define MOE_MAX_H 24576
 
 typedef struct {

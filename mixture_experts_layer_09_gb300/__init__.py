@@ -22,7 +22,8 @@ from typing import Optional
 from . import _build
 
 ARM_AUTO, ARM_GEMV, ARM_GEMM = 0, 1, 2
-AUTO_GEMV_MAX_T = 32
+AUTO_GEMV_ROWS_PER_EXPERT = 4   # MOE_AUTO_GEMV_ROWS_PER_EXPERT
+AUTO_GEMV_MAX_T_SHARED = 16     # MOE_AUTO_GEMV_MAX_T_SHARED
 
 _lib = None
 

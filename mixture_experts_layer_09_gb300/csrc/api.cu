@@ -134,12 +134,17 @@ int check_shared(const moe_shared* sh) {
     return MOE_OK;
 }
 
-int choose_arm(int arm, int T, int H, int I, int I_sh) {
+// AUTO: the bandwidth arm while the batch puts at most a few rows on an expert (and on the
+// shared expert, which takes every token), else the tensor arm -- the crossover measured by
+// sweeping both arms over T.
+int choose_arm(int arm, int T, int k, int E, int H, int I, int I_sh) {
     const bool gemm_ok = gemm_supported(H, I, I_sh);
     if (arm == MOE_ARM_GEMV) return MOE_ARM_GEMV;
     if (arm == MOE_ARM_GEMM) return gemm_ok ? MOE_ARM_GEMM : -1;
     if (arm != MOE_ARM_AUTO) return -1;
-    if (T <= MOE_AUTO_GEMV_MAX_T || !gemm_ok) return MOE_ARM_GEMV;
+    const bool few_rows = static_cast<long long>(T) * k <= static_cast<long long>(MOE_AUTO_GEMV_ROWS_PER_EXPERT) * E &&
+                          (I_sh <= 0 || T <= MOE_AUTO_GEMV_MAX_T_SHARED);
+    if (few_rows || !gemm_ok) return MOE_ARM_GEMV;
     return MOE_ARM_GEMM;
 }
 
@@ -356,7 +361,7 @@ int moe_expert_mlp(const uint16_t* x, int T, int k, const moe_experts* W, const 
     if (!x || !offsets || !perm || !rows || !ws || !aligned16(x) || !aligned16(rows)) return MOE_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_expert_mlp_workspace_size(T, k, W->E, W->H, W->I)) return MOE_ERR_INVALID_ARG;
-    const int a = choose_arm(arm, T, W->H, W->I, 0);
+    const int a = choose_arm(arm, T, k, W->E, W->H, W->I, 0);
     if (a < 0) return arm == MOE_ARM_AUTO || arm == MOE_ARM_GEMV || arm == MOE_ARM_GEMM ? MOE_ERR_UNSUPPORTED
                                                                                       : MOE_ERR_INVALID_ARG;
     if (int s = check_device()) return s;
@@ -419,7 +424,7 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
     const int I_sh = sh ? sh->I_sh : 0;
     if (ws_bytes < moe_workspace_size(T, W->E, k, W->H, W->I, I_sh)) return MOE_ERR_INVALID_ARG;
-    const int a = choose_arm(arm, T, W->H, W->I, I_sh);
+    const int a = choose_arm(arm, T, k, W->E, W->H, W->I, I_sh);
     if (a < 0) return arm == MOE_ARM_AUTO || arm == MOE_ARM_GEMV || arm == MOE_ARM_GEMM ? MOE_ERR_UNSUPPORTED
                                                                                       : MOE_ERR_INVALID_ARG;
     if (int s = check_device()) return s;
@@ -439,16 +444,18 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     if (a == MOE_ARM_GEMV) {
         GemvBufs b;
         carve_gemv(c, T, k, W->H, W->I, I_sh, b);
-        // decode batches: 4 launches -- logits (+ x quantisation), top-k + dispatch, gate/up, down + combine
+        // decode batches: 3 launches -- logits + x quantisation + top-k + dispatch, gate/up, down + combine
         const bool fused_routing = T <= 32;
-        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H), status) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+        DecodeRoute dr;
         if (fused_routing) {
-            if (launch_topk_dispatch(r.logits, ld, T, W->E, k, ids, w, r.counts, r.offsets, r.perm, r.inv, r.active,
-                                     r.n_active, status, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
-        } else {
+            dr.k = k; dr.ids = ids; dr.w = w; dr.counts = r.counts; dr.offsets = r.offsets; dr.perm = r.perm;
+            dr.inv = r.inv; dr.active = r.active; dr.n_active = r.n_active; dr.status = status;
+            dr.done = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + kWsRouteOffset);
+        }
+        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H), status,
+                                 fused_routing ? &dr : nullptr) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (!fused_routing) {
             if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
             if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active,
                                 r.disp_scratch, status, st) != cudaSuccess)

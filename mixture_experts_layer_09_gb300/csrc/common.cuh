@@ -23,6 +23,7 @@ constexpr size_t kWsAlign = 256;
 constexpr size_t kWsHead = 4096;
 constexpr size_t kWsCounterOffset = 1024;
 constexpr size_t kWsTaskOffset = 512;  // GEMV task claim counters (4 ints)
+constexpr size_t kWsRouteOffset = 528;  // decode routing: row-CTA completion count (1 int)
 constexpr int kMaxColBlocks = static_cast<int>((kWsHead - kWsCounterOffset) / sizeof(int));  // H <= 24576
 
 // Device status word layout (first 256 bytes of every workspace).

@@ -100,62 +100,6 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     warp_walk(ids, begin, end, E, hist + w * E, 1, perm, inv, status);
 }
 
-// Decode batches (T <= 32): one CTA computes the top-k of every token (warp t takes token t)
-// and then the dispatch of the fresh ids -- stages 1 and 2 in one launch.
-template <int VPT>
-__global__ void __launch_bounds__(1024) topk_dispatch_kernel(const float* __restrict__ logits, int ld, int T, int E,
-                                                             int k, int32_t* ids, float* w, int32_t* counts,
-                                                             int32_t* offsets, int32_t* perm, int32_t* inv,
-                                                             int32_t* active, int32_t* n_active, int* status) {
-    pdl_wait();
-    pdl_trigger();
-    // the ids stay in shared memory between the top-k and the two walks; warp r walks slots
-    // 32r .. 32r+31, so only ceil(T*k / 32) histogram rows are in use
-    extern __shared__ int hist[];  // [rows][E]
-    __shared__ int ids_s[1024];
-    __shared__ int scratch[9];
-    const int wid = threadIdx.x >> 5;
-    const int n = T * k;
-    const int rows = (n + 31) / 32;
-    for (int i = threadIdx.x; i < rows * E; i += blockDim.x) hist[i] = 0;
-    if (wid < T)
-        topk_warp_row<float, VPT>(logits + static_cast<size_t>(wid) * ld, E, k, ids_s + wid * k,
-                                  w + static_cast<size_t>(wid) * k);
-    __syncthreads();
-    if (static_cast<int>(threadIdx.x) < n) ids[threadIdx.x] = ids_s[threadIdx.x];
-    const int begin = min(n, wid * 32), end = min(n, begin + 32);
-    warp_walk(ids_s, begin, end, E, hist + wid * E, 0, perm, inv, status, true);
-    __syncthreads();
-    finalize_plan(hist, rows, E, n, counts, offsets, active, n_active, scratch);
-    __syncthreads();
-    warp_walk(ids_s, begin, end, E, hist + wid * E, 1, perm, inv, status, true);
-}
-
-cudaError_t launch_topk_dispatch(const float* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
-                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
-                                 int32_t* n_active, int* status, cudaStream_t st) {
-    const size_t smem = static_cast<size_t>((T * k + 31) / 32) * E * sizeof(int);
-    const int vpt = (E + 31) / 32;
-    KernelScope ks_("topk_dispatch", st);
-    switch (vpt) {
-#define MOE_TD_CASE(V)                                                                                            \
-    case V:                                                                                                       \
-        return launch_pdl(topk_dispatch_kernel<V>, dim3(1), dim3(1024), smem, st, logits, ld, T, E, k, ids, w,  \
-                          counts, offsets, perm, inv, active, n_active, status);
-        MOE_TD_CASE(1)
-        MOE_TD_CASE(2)
-        MOE_TD_CASE(3)
-        MOE_TD_CASE(4)
-        MOE_TD_CASE(5)
-        MOE_TD_CASE(6)
-        MOE_TD_CASE(7)
-        MOE_TD_CASE(8)
-#undef MOE_TD_CASE
-        default:
-            return cudaErrorInvalidValue;
-    }
-}
-
 size_t dispatch_scratch_bytes(int n, int E) {
     if (n <= kSmallSlots) return 0;
     const size_t nblk = (n + kBigSlotsPerCta - 1) / kBigSlotsPerCta;

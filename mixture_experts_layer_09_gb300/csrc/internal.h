@@ -26,10 +26,27 @@ bool tmap_2d(CUtensorMap* out, CUtensorMapDataType dtype, const void* base, uint
              uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 // router.cu
-// xq/xsc/xsum (optional): also quantise x for the GEMV arm in the same launch (decode batches).
+// Decode routing in the logits launch (T <= 32): top-k ids/w of every token and the dispatch
+// (counts, offsets, perm, inv, active list), run by the row CTA that finishes last; `done` is a
+// completion count that is zero between calls (workspace head).
+struct DecodeRoute {
+    int k = 0;
+    int32_t* ids = nullptr;       // null: logits only
+    float* w = nullptr;
+    int32_t* counts = nullptr;
+    int32_t* offsets = nullptr;
+    int32_t* perm = nullptr;
+    int32_t* inv = nullptr;
+    int32_t* active = nullptr;
+    int32_t* n_active = nullptr;
+    int* status = nullptr;
+    int* done = nullptr;
+};
+// xq/xmeta (optional): also quantise x for the GEMV arm in the same launch (decode batches).
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
                                  int E, float* logits, cudaStream_t st, int16_t* xq = nullptr,
-                                 int2* xmeta = nullptr, int x_gld = 0, int* status = nullptr);
+                                 int2* xmeta = nullptr, int x_gld = 0, int* status = nullptr,
+                                 const DecodeRoute* route = nullptr);
 // router_tc.cu: tcgen05 logits GEMM for T > 32 (status: device timeout record, may be null)
 // (H % 64 == 0, 1 <= E <= 256, x / W_r / g 16-byte aligned)
 bool router_tc_supported(const void* x, const void* W_r, const void* g, int H, int E);
@@ -43,10 +60,6 @@ cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, 
                                float scale = 1.f);
 
 // dispatch.cu
-// Decode batches (T <= 32): top-k of every token and the dispatch in one single-CTA launch.
-cudaError_t launch_topk_dispatch(const float* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
-                                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
-                                 int32_t* n_active, int* status, cudaStream_t st);
 size_t dispatch_scratch_bytes(int n_slots, int E);
 cudaError_t launch_dispatch(const int32_t* ids, int n_slots, int E, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* scratch,

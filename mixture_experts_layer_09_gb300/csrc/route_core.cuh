@@ -19,6 +19,15 @@ template <>
 __device__ __forceinline__ float load_logit<float>(const float* p) { return __ldg(p); }
 template <>
 __device__ __forceinline__ float load_logit<uint16_t>(const uint16_t* p) { return bf16_to_f32(__ldg(p)); }
+// fp32 logits written earlier by other CTAs of the same kernel: coherent loads through L2
+struct CoherentF32 {
+    float v;
+};
+static_assert(sizeof(CoherentF32) == sizeof(float), "one logit per element");
+template <>
+__device__ __forceinline__ float load_logit<CoherentF32>(const CoherentF32* p) {
+    return __ldcg(reinterpret_cast<const float*>(p));
+}
 
 // VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
 // One warp selects the top-k of one logit row.  ids/w receive the row's k outputs.

@@ -24,12 +24,14 @@ namespace moe {
 // dots it with every token in one pass (TB >= T); 256 threads, one 16-byte chunk of the row
 // per thread per 2048 columns; the eight warp sums meet in a fixed order.  CTAs past the rows
 // quantise x for the GEMV arm (one 32-value group per warp) when xq != nullptr, so that step
-// costs no launch of its own.
-template <int TB>
+// costs no launch of its own.  With routing (r.ids != nullptr) the row CTA that finishes last
+// (a completion count after a release fence) also runs the softmax top-k of every token and
+// the dispatch of the fresh ids, so a decode batch routes in this one launch.
+template <int TB, int VPT>
 __global__ void __launch_bounds__(256) router_logits_gemv_kernel(
     const uint16_t* __restrict__ x, const uint16_t* __restrict__ W_r, const uint16_t* __restrict__ g,
     int T, int H, int E, int ld, float* __restrict__ logits, int nrows, int16_t* __restrict__ xq,
-    int2* __restrict__ xmeta, int x_gld) {
+    int2* __restrict__ xmeta, int x_gld, DecodeRoute r) {
     pdl_wait();
     pdl_trigger();
     const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -83,6 +85,34 @@ __global__ void __launch_bounds__(256) router_logits_gemv_kernel(
         logits[static_cast<size_t>(i) * ld + row] =
             ((red[0][i] + red[1][i]) + (red[2][i] + red[3][i])) + ((red[4][i] + red[5][i]) + (red[6][i] + red[7][i]));
     }
+    if (!r.ids) return;
+    // ---- the last row CTA routes the batch
+    __shared__ int is_last;
+    __threadfence();  // this CTA's logits, before its count
+    __syncthreads();
+    if (threadIdx.x == 0) is_last = atomicAdd(r.done, 1) == nrows - 1;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    extern __shared__ int dyn[];  // [T*k] ids | [rows][E] walk counts, rows = ceil(T*k / 32)
+    const int k = r.k, n = T * k, rows = (n + 31) / 32;
+    int* ids_s = dyn;
+    int* hist = dyn + ((n + 3) & ~3);
+    __shared__ int scratch[9];
+    for (int i = threadIdx.x; i < rows * E; i += blockDim.x) hist[i] = 0;
+    for (int t = wid; t < T; t += 8)
+        topk_warp_row<CoherentF32, VPT>(reinterpret_cast<const CoherentF32*>(logits + static_cast<size_t>(t) * ld), E, k,
+                                        ids_s + t * k, r.w + static_cast<size_t>(t) * k);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) r.ids[i] = ids_s[i];
+    for (int q = wid; q < rows; q += 8)
+        warp_walk(ids_s, q * 32, min(n, q * 32 + 32), E, hist + q * E, 0, r.perm, r.inv, r.status, true);
+    __syncthreads();
+    finalize_plan(hist, rows, E, n, r.counts, r.offsets, r.active, r.n_active, scratch);
+    __syncthreads();
+    for (int q = wid; q < rows; q += 8)
+        warp_walk(ids_s, q * 32, min(n, q * 32 + 32), E, hist + q * E, 1, r.perm, r.inv, r.status, true);
+    if (threadIdx.x == 0) *r.done = 0;  // ready for the next call
 }
 
 // ------------------------------------------------------------------ logits, prefill GEMM
@@ -156,26 +186,30 @@ __global__ void __launch_bounds__(256) router_logits_gemm_kernel(
 
 cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H,
                                  int E, float* logits, cudaStream_t st, int16_t* xq, int2* xmeta, int x_gld,
-                                 int* status) {
+                                 int* status, const DecodeRoute* route) {
     if (x_gld == 0) x_gld = H / 32;
     if (T == 0) return cudaSuccess;
     const int nrows = E + (g ? 1 : 0);
     const int ld = nrows;
     if (T <= 32) {
         const int qctas = xq ? (T * (H / 32) + 7) / 8 : 0;
-        KernelScope ks_(xq ? "router_logits_gemv+quant_x" : "router_logits_gemv", st);
+        const DecodeRoute r = route ? *route : DecodeRoute{};
+        const size_t smem = r.ids ? sizeof(int) * (((T * r.k + 3) & ~3) + static_cast<size_t>((T * r.k + 31) / 32) * E)
+                                  : 0;
+        KernelScope ks_(r.ids ? "router_gemv+topk+dispatch" : (xq ? "router_logits_gemv+quant_x" : "router_logits_gemv"),
+                        st);
         const dim3 grid(nrows + qctas), block(256);
-        if (T <= 4)
-            return launch_pdl(router_logits_gemv_kernel<4>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
-                              xq, xmeta, x_gld);
-        if (T <= 8)
-            return launch_pdl(router_logits_gemv_kernel<8>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
-                              xq, xmeta, x_gld);
-        if (T <= 16)
-            return launch_pdl(router_logits_gemv_kernel<16>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows,
-                              xq, xmeta, x_gld);
-        return launch_pdl(router_logits_gemv_kernel<32>, grid, block, 0, st, x, W_r, g, T, H, E, ld, logits, nrows, xq,
-                          xmeta, x_gld);
+        const int vpt = E <= 64 ? 2 : (E <= 128 ? 4 : 8);
+#define MOE_RG_CASE(TBV, V)                                                                                     \
+    if (T <= TBV && vpt == V)                                                                                   \
+        return launch_pdl(router_logits_gemv_kernel<TBV, V>, grid, block, smem, st, x, W_r, g, T, H, E, ld, logits, \
+                          nrows, xq, xmeta, x_gld, r);
+        MOE_RG_CASE(4, 2) MOE_RG_CASE(4, 4) MOE_RG_CASE(4, 8)
+        MOE_RG_CASE(8, 2) MOE_RG_CASE(8, 4) MOE_RG_CASE(8, 8)
+        MOE_RG_CASE(16, 2) MOE_RG_CASE(16, 4) MOE_RG_CASE(16, 8)
+        MOE_RG_CASE(32, 2) MOE_RG_CASE(32, 4) MOE_RG_CASE(32, 8)
+#undef MOE_RG_CASE
+        return cudaErrorInvalidValue;
     }
     cudaError_t e;
     if (router_tc_supported(x, W_r, g, H, E)) {

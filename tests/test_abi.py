@@ -132,3 +132,14 @@ def test_no_cpu_fallback_without_device(L):
     fake = C.c_void_p(0x1000)
     rc = L.moe_router_topk(fake, 0, 8, 4, 8, 2, fake, fake, None)
     assert rc in (-3, -2)
+
+
+def test_auto_arm_constants_match_the_header():
+    """The binding's copy of the AUTO arm rule's constants equals the header's."""
+    import re
+
+    import mixture_experts_layer_09_gb300 as moe
+    hdr = open(os.path.join(ROOT, "include", "moe.h")).read()
+    vals = dict(re.findall(r"#define (MOE_AUTO_GEMV_\w+) (\d+)", hdr))
+    assert int(vals["MOE_AUTO_GEMV_ROWS_PER_EXPERT"]) == moe.AUTO_GEMV_ROWS_PER_EXPERT
+    assert int(vals["MOE_AUTO_GEMV_MAX_T_SHARED"]) == moe.AUTO_GEMV_MAX_T_SHARED
