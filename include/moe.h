@@ -261,12 +261,26 @@ MOE_API int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, 
                                    size_t ws_bytes, moe_stream_t stream);
 
 /* Clears the head of a workspace (its first 4096 bytes: the device status word, the GEMV
- * arm's task claim counters and the down projection's column counters) on `stream`.  A
- * workspace must start with a zero head: call this once on a new workspace, or allocate it
- * zero-filled.  The calls above leave the head zero again (except a recorded status); after
- * a call that recorded MOE_ERR_DEVICE_TIMEOUT the counters may not be zero, so call this
- * again before reusing the workspace. */
+ * arm's task claim counters, the decode routing's completion count, the down projection's
+ * column counters and the test hook below) on `stream`.  A workspace must start with a zero
+ * head: call this once on a new workspace, or allocate it zero-filled.  The calls above leave
+ * the head zero again (except a recorded status); after a call that recorded
+ * MOE_ERR_DEVICE_TIMEOUT the counters may not be zero, so call this again before reusing the
+ * workspace. */
 MOE_API int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Test support for the bounded device waits (a device-side wait gives up, records a status
+ * and lets its kernel return instead of hanging the GPU).  Sets the workspace's
+ * test hook on `stream`: the next calls that run the tensor arm's gate/up kernel with this
+ * workspace use wait_limit_cycles (> 0; 0 keeps the default of about two seconds) as the
+ * limit of its waits, and its first CTA withholds the token-tile copy of its second K-step,
+ * so that its MMA thread's wait runs out: that CTA records MOE_ERR_DEVICE_TIMEOUT in the
+ * status word, every role of it stops, it waits (bounded) for its own copies and MMAs, frees
+ * its tensor memory and returns; the rest of the call runs to completion with that CTA's
+ * share of the output unspecified.  moe_workspace_init clears the hook.  Returns
+ * MOE_ERR_INVALID_ARG for a null, short or misaligned workspace or a negative limit. */
+MOE_API int moe_workspace_test_timeout(void* ws, size_t ws_bytes, long long wait_limit_cycles,
+                                       moe_stream_t stream);
 
 /* Synchronises `stream`, copies the device status word of a workspace used by
  * the calls above into *status (MOE_OK or a MOE_ERR_DEVICE_* code) and clears

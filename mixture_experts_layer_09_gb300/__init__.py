@@ -78,6 +78,7 @@ _SIGS = {
     "moe_layer_forward_norm": (_I, [_P, _P, _P, C.POINTER(moe_experts), C.POINTER(moe_shared), _I, _I, _P, _P,
                                     C.c_float, _P, _P, _P, _I, _P, _S, _P]),
     "moe_workspace_init": (_I, [_P, _S, _P]),
+    "moe_workspace_test_timeout": (_I, [_P, _S, C.c_longlong, _P]),
     "moe_mxfp4_scales": (_I, [_P, _S, _P, _P, _S, _P]),
     "moe_device_status": (_I, [_P, _S, C.POINTER(C.c_int), _P]),
     "moe_launch_count": (C.c_longlong, []),
@@ -351,6 +352,14 @@ def moe_rmsnorm(y, gamma, eps: float, y_norm, stream=None):
 
 def moe_workspace_init(ws, stream=None):
     _check(lib().moe_workspace_init(_ptr(ws), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
+def moe_workspace_test_timeout(ws, wait_limit_cycles: int, stream=None):
+    """Test hook: the next tensor-arm gate/up kernel on this workspace uses this wait limit and
+    withholds one copy in its first CTA, so a bounded wait runs out (cleared by
+    moe_workspace_init)."""
+    _check(lib().moe_workspace_test_timeout(_ptr(ws), ws.numel(), int(wait_limit_cycles), _stream(stream)),
+           "moe_workspace_test_timeout")
 
 
 def moe_device_status(ws, stream=None) -> int:

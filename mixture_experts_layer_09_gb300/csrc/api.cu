@@ -501,6 +501,30 @@ int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const ui
     return status_of(launch_rmsnorm(y, norm_gamma, T, W->H, eps, y_norm, S(stream)));
 }
 
+}  // extern "C"
+
+namespace {
+__global__ void write_test_hook_kernel(TestHook* hook, long long wait_limit, int withhold) {
+    pdl_wait();
+    pdl_trigger();
+    hook->wait_limit = wait_limit;
+    hook->withhold_copy = withhold;
+    hook->pad = 0;
+}
+}  // namespace
+
+extern "C" {
+
+int moe_workspace_test_timeout(void* ws, size_t ws_bytes, long long wait_limit_cycles, moe_stream_t stream) {
+    if (!ws || ws_bytes < kWsHead || wait_limit_cycles < 0) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
+    if (int s = check_device()) return s;
+    cudaStream_t st = S(stream);
+    TestHook* hook = reinterpret_cast<TestHook*>(static_cast<char*>(ws) + kWsTestHookOffset);
+    KernelScope ks_("write_test_hook", st);
+    return status_of(launch_pdl(write_test_hook_kernel, dim3(1), dim3(1), 0, st, hook, wait_limit_cycles, 1));
+}
+
 int moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
     if (!ws || ws_bytes < kWsHead) return MOE_ERR_INVALID_ARG;
     return status_of(cudaMemsetAsync(ws, 0, kWsHead, S(stream)));

@@ -38,17 +38,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait: false when the CTA is aborting or the limit ran out (then it records the
-// timeout and raises the abort flag for every role of the CTA).
+// Bounded wait: false when the CTA is aborting or the limit (clock cycles) ran out (then it
+// records the timeout and raises the abort flag for every role of the CTA).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, int where) {
+                                          int* status, int where, long long limit = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 255) == 0) {
             if (*abort_flag) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
+            if (clock64() - t0 > limit) {
                 *abort_flag = 1;
                 record_status(status, MOE_ERR_DEVICE_TIMEOUT, where, static_cast<int>(blockIdx.x));
                 return false;

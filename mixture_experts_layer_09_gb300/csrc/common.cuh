@@ -24,6 +24,15 @@ constexpr size_t kWsHead = 4096;
 constexpr size_t kWsCounterOffset = 1024;
 constexpr size_t kWsTaskOffset = 512;  // GEMV task claim counters (4 ints)
 constexpr size_t kWsRouteOffset = 528;  // decode routing: row-CTA completion count (1 int)
+// Test hook (16 bytes, zero in normal use): a wait limit in clock cycles (int64, 0 = the
+// default) and an int that makes the tensor arm's gate/up kernel withhold one token-tile copy
+// in its first CTA, so that a bounded wait runs out (moe_workspace_test_timeout).
+constexpr size_t kWsTestHookOffset = 544;
+struct TestHook {
+    long long wait_limit;
+    int withhold_copy;
+    int pad;
+};
 constexpr int kMaxColBlocks = static_cast<int>((kWsHead - kWsCounterOffset) / sizeof(int));  // H <= 24576
 
 // Device status word layout (first 256 bytes of every workspace).

@@ -232,6 +232,11 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
     pdl_trigger();
     constexpr int S = kGuStages;
     constexpr int CPT = 8 / kGuTpr;
+    // the workspace's test hook (zero in normal use): a shorter wait limit, and a token-tile copy
+    // that the first CTA withholds so that its MMA thread's wait runs out
+    const TestHook hook = *reinterpret_cast<const TestHook*>(reinterpret_cast<const char*>(p.status) + kWsTestHookOffset);
+    const long long wl = hook.wait_limit > 0 ? hook.wait_limit : kWaitLimitCycles;
+    const bool withhold = hook.withhold_copy != 0 && blockIdx.x == 0;
     Item w;
     if (!item_at(p, blockIdx.x, __ldg(p.n_tiles), w)) return;  // no rows: nothing to do
     const int nk = w.K / BK;
@@ -275,16 +280,16 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
         for (int kb = 0; kb < nk; ++kb) {
             const int s = kb % S;
             bool ok = true;
-            if (kb >= S && lane == 0) ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 1);
+            if (kb >= S && lane == 0) ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 1, wl);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-            load_b_stage(stage_b(s), tm, kb, brow, w.nrows, full_b + s, lane);
+            if (!(withhold && kb == 1)) load_b_stage(stage_b(s), tm, kb, brow, w.nrows, full_b + s, lane);
             issued = kb + 1;
         }
         if (*abort_flag && lane == 0) {
             // let the copies this warp started land before the CTA leaves
             for (int kb = max(0, issued - S); kb < issued; ++kb) {
                 const long long t0 = clock64();
-                while (!mbar_try_wait(full_b + kb % S, (kb / S) & 1) && clock64() - t0 < kWaitLimitCycles) {
+                while (!mbar_try_wait(full_b + kb % S, (kb / S) & 1) && clock64() - t0 < wl) {
                 }
             }
         }
@@ -296,8 +301,8 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
             for (int kb = 0; kb < nk; ++kb) {
                 const int s = kb % S;
                 const uint32_t par = (kb / S) & 1;
-                if (!mbar_wait(full_b + s, par, abort_flag, p.status, 2)) break;
-                if (!mbar_wait(full_a + s, par, abort_flag, p.status, 3)) break;
+                if (!mbar_wait(full_b + s, par, abort_flag, p.status, 2, wl)) break;
+                if (!mbar_wait(full_a + s, par, abort_flag, p.status, 3, wl)) break;
                 tc_fence_after();
                 const uint32_t b0 = smem_u32(stage_b(s));
 #pragma unroll
@@ -316,7 +321,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
             } else if (any) {
                 mma_commit(drain);  // wait for this thread's MMAs before tensor memory is freed
                 const long long t0 = clock64();
-                while (!mbar_try_wait(drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+                while (!mbar_try_wait(drain, 0) && clock64() - t0 < wl) {
                 }
             }
         }
@@ -349,7 +354,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
                 const int s = kb % S;
                 if (kb >= S) {
                     bool free_ok = true;
-                    if (lane == 0) free_ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4);
+                    if (lane == 0) free_ok = mbar_wait(empty + s, ((kb / S) & 1) ^ 1, abort_flag, p.status, 4, wl);
                     if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
                         ok = false;
                         break;
@@ -370,7 +375,7 @@ __global__ void __launch_bounds__(kGuThreads, 1) moe_gateup_kernel(const __grid_
         // is staged in the pipeline's shared memory (free once the accumulators are final) as
         // fp16 h in the down GEMM's K order, then each thread writes one token row by bulk copy.
         bool go = __all_sync(0xffffffffu, ok);
-        if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5));
+        if (go) go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 5, wl));
         go = named_barrier_or(2, kGuDqThreads, !go) ? false : go;  // all epilogue warps agree
         if (go) {
             tc_fence_after();
