@@ -200,8 +200,9 @@ MOE_API int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* 
  * exits), and allocates nothing.
  *   Arguments and outputs are those of moe_dispatch; T*k must not exceed
  *   MOE_DISPATCH_STATIC_MAX_SLOTS (else MOE_ERR_INVALID_ARG, nothing enqueued).
- *   The first call on a device looks up the array's device address (once per device, with
- *   that device current); make that first call before any stream capture.
+ *   A call looks up the array's device address on the current device (again on every call
+ *   whose stream is not being captured, so a device reset does not leave a stale address);
+ *   make the first call on a device before any stream capture.
  *   Every call on a device shares the one array and each call clears its status word first:
  *   calls that overlap on the GPU (other streams, other host threads) race and must be
  *   serialised by the caller.  An id outside [0, E) is left out of every bucket (its inv

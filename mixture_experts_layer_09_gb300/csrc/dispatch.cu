@@ -170,13 +170,17 @@ std::mutex g_static_mu;
 void* g_static_addr[kMaxDevices] = {};
 
 // Device address of g_dispatch_scratch on the current device.  The name is only a host-side
-// stand-in for the array, so the address is looked up once per device (with that device
-// current) and cached.
-int static_scratch_address(void** out) {
+// stand-in for the array, so the address is looked up with that device current.  It is looked
+// up again on every call whose stream is not being captured (a device reset reloads the
+// library's module, which moves the array), and the last address is kept for calls made while
+// a capture is in progress, where the lookup is not made.
+int static_scratch_address(cudaStream_t st, void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_addr[dev]) {
+    if (cap == cudaStreamCaptureStatusNone || !g_static_addr[dev]) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_dispatch_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
         g_static_addr[dev] = p;
@@ -198,7 +202,7 @@ extern "C" MOE_API int moe_dispatch_static(const int32_t* topk_ids, int T, int k
         return MOE_ERR_CUDA;
     if (major != 10 || minor != 3) return MOE_ERR_UNSUPPORTED;
     void* base = nullptr;
-    if (int s = static_scratch_address(&base)) return s;
+    if (int s = static_scratch_address(static_cast<cudaStream_t>(stream), &base)) return s;
     char* p = static_cast<char*>(base);
     int* status = reinterpret_cast<int*>(p);
     int32_t* active = reinterpret_cast<int32_t*>(p + moe::kStaticStatusBytes);

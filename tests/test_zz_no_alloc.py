@@ -4,7 +4,8 @@ time -- must give the same buckets as moe_dispatch with a caller workspace.
 The variant keeps its scratch in one array inside the library that every call on the device
 shares, so the check runs two calls in a row with different inputs: the second must not see
 anything left over from the first.  Both the one-CTA path and the multi-CTA path (which uses
-the per-CTA count table) are covered.  This file is collected last on purpose."""
+the per-CTA count table) are covered.  The file is collected last so that, if it fails, a run
+that stops at the first failure has already run every other test."""
 import ctypes as C
 
 import numpy as np
@@ -61,3 +62,31 @@ def test_static_dispatch_rejects_oversize(moe):
     T, k = (1 << 20) // 8 + 1, 8  # one token past the fixed array's capacity
     assert L.moe_dispatch_static(fake, T, k, 256, None, fake, fake, fake, None) == -1
     torch.cuda.synchronize()
+
+
+def test_static_dispatch_out_of_range_ids_and_empty_batch(moe):
+    """The documented edge behaviour: an id outside [0, E) lands in no bucket and its inv entry
+    is -1; T = 0 is accepted with null id, perm and inv pointers and gives zero offsets."""
+    import torch
+    L = moe.lib()
+    T, k, E = 5, 2, 8
+    ids_np = _ids(9, T, E, k)
+    ids_np[1, 0] = -1
+    ids_np[3, 1] = E
+    ids = torch.from_numpy(ids_np).cuda()
+    counts, offsets, perm, inv = _outputs(torch, T, k, E)
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.moe_dispatch_static(ids.data_ptr(), T, k, E, counts.data_ptr(), offsets.data_ptr(), perm.data_ptr(),
+                                 inv.data_ptr(), stream) == 0
+    torch.cuda.synchronize()
+    inv_np = inv.cpu().numpy()
+    assert inv_np[1 * k + 0] == -1 and inv_np[3 * k + 1] == -1
+    assert int(offsets[E]) == T * k - 2
+    valid = [a for a in range(T * k) if a not in (1 * k + 0, 3 * k + 1)]
+    assert sorted(perm.cpu().numpy()[:T * k - 2].tolist()) == valid
+    # empty batch: no ids, no perm, no inv
+    counts0, offsets0, _, _ = _outputs(torch, 1, 1, E)
+    assert L.moe_dispatch_static(None, 0, k, E, counts0.data_ptr(), offsets0.data_ptr(), None, None, stream) == 0
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(offsets0).item() == 0
+    assert torch.count_nonzero(counts0).item() == 0
