@@ -142,6 +142,27 @@ def test_layer_qwen15_prefill_t4096(moe):
 
 
 @pytest.mark.parametrize("arm", [2, 1])
+def test_layer_same_bits_on_repeat(moe, arm):
+    """Both arms sum each token in one fixed order (gated shared row, slots in order, residual)
+    whichever CTA finishes last: repeated calls on one workspace (the bandwidth arm's later calls
+    starting from the column counters the earlier left) give the same bits, and match the oracle."""
+    import torch
+    inp = wk.layer("qwen15_prefill_t512", T=512 if arm == 2 else 16)
+    wl = inp.wl
+    x, r, W_r, E, S = wk.upload(inp)
+    ws = torch.zeros(moe.moe_workspace_size(wl.T, wl.E, wl.k, wl.H, wl.I, S.I_sh), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        y = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda"))
+        moe.moe_layer_forward(x, r, W_r, E, S, wl.k, y, ws, arm=arm)
+        outs.append(y.cpu().numpy())
+    assert moe.moe_device_status(ws) == 0
+    assert all(np.array_equal(o.view(np.uint32), outs[0].view(np.uint32)) for o in outs[1:])
+    ref = oracle.layer_forward(inp)
+    wk.assert_close(outs[0], ref["y"], f"y arm={arm}")
+
+
+@pytest.mark.parametrize("arm", [2, 1])
 def test_expert_mlp_rows_qwen15_t512_every_row(moe, arm):
     """moe_expert_mlp at the full prefill shape (H=2048, I=1408, E=60, k=4, T=512): all 2,048
     dispatched rows, every element, unweighted in dispatch order."""
