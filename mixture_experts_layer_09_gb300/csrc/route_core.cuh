@@ -10,9 +10,11 @@ namespace moe {
 // ------------------------------------------------------------------ softmax top-k
 // One warp per token with the whole logit row in registers, no shared memory, one read of the
 // row (vllm.cpp PR #481 "gate(#378): the first DEVICE run of the warp MoE router", warp-router
-// commit).  Selection is k rounds of a warp argmax with the lowest index winning a tie;
-// weights are the fp32 softmax over all E logits renormalised over the k picks; the picks are
-// written in ascending expert id.
+// commit).  Selection is k rounds of a warp argmax with the lowest index winning a tie (per
+// round one warp max over order-preserving integer keys of the scores and one warp min over
+// the indices holding it); weights are the fp32 softmax over all E logits renormalised over
+// the k picks -- computed as the softmax over the picked logits, which it equals -- or, for the
+// unnormalised variant, the full softmax; the picks are written in ascending expert id.
 template <typename Tin>
 __device__ __forceinline__ float load_logit(const Tin* p);
 template <>
@@ -38,86 +40,92 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
                                               float* __restrict__ w, const float* __restrict__ bias = nullptr,
                                               bool renorm = true, float scale = 1.f) {
     const int lane = threadIdx.x & 31;
-    float v[VPT];   // logits: the softmax
-    float sv[VPT];  // selection scores: logit + bias
-    bool picked[VPT];
+    float v[VPT];         // logits: the softmax
+    uint32_t key[VPT];    // selection scores (logit + bias) as order-preserving integers; 0 once picked
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int e = lane + 32 * j;
         if (e < E) {
             float f = load_logit<Tin>(row + e);
             v[j] = (f != f) ? -INFINITY : f;  // NaN never wins a pick
-            const float sb = bias ? v[j] + __ldg(bias + e) : v[j];
-            sv[j] = (sb != sb) ? -INFINITY : sb;
-            picked[j] = false;
+            float sb = bias ? v[j] + __ldg(bias + e) : v[j];
+            sb = (sb != sb) ? -INFINITY : sb + 0.f;  // + 0 folds -0 into +0: the two are equal scores
+            const uint32_t u = __float_as_uint(sb);
+            key[j] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);  // -inf -> 0x007fffff, above 0
         } else {
             v[j] = -INFINITY;
-            sv[j] = -INFINITY;
-            picked[j] = true;  // padding is never a candidate
+            key[j] = 0u;  // padding is never a candidate
         }
     }
-    // k rounds of a warp argmax: larger value first, lower expert index on a tie.
+    // k rounds: the largest score (one warp max over the keys), then the lowest expert index
+    // holding it (one warp min); the pick's key becomes 0, and a maximum of 0 means no candidate.
     for (int round = 0; round < k; ++round) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        uint32_t bk = 0u;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) bk = max(bk, key[j]);
+        const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+        if (gk == 0u) break;  // warp-uniform
+        int cand = 0x7fffffff;
+#pragma unroll
+        for (int j = VPT - 1; j >= 0; --j)  // lane + 32 j grows with j: the last match kept is the lowest
+            if (key[j] == gk) cand = lane + 32 * j;
+        const int bi = __reduce_min_sync(0xffffffffu, cand);
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            if (bi == lane + 32 * j) key[j] = 0u;
+    }
+    bool picked[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) picked[j] = key[j] == 0u && lane + 32 * j < E;
+    float p[VPT];
+    if (renorm) {
+        // the softmax over all E renormalised over the picks is the softmax over the picked
+        // logits alone: k exponentials, shifted by the largest picked logit
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            if (picked[j]) m = fmaxf(m, v[j]);
+        m = warp_max(m);
+        float z = 0.f;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
-            const int e = lane + 32 * j;
-            if (!picked[j] && (sv[j] > bv || (sv[j] == bv && e < bi))) {
-                bv = sv[j];
-                bi = e;
-            }
+            p[j] = 0.f;
+            if (picked[j] && m > -INFINITY) p[j] = expf(v[j] - m);  // a lane holds few picks
+            z += p[j];
         }
+        z = warp_sum(z);
+        // denominator guard: a row with no finite picked logit spreads the weight evenly
+        const float rz = (z > 0.f) ? 1.f / z : 0.f;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
+        for (int j = 0; j < VPT; ++j) p[j] = (z > 0.f) ? p[j] * rz : 1.f / k;
+    } else {
+        // fp32 softmax over all E logits
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j)
+            if (lane + 32 * j < E) m = fmaxf(m, v[j]);
+        m = warp_max(m);
+        float z = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            p[j] = (lane + 32 * j < E && m > -INFINITY) ? expf(v[j] - m) : 0.f;
+            z += p[j];
         }
-        if (bi != 0x7fffffff && (bi & 31) == lane) {
+        z = warp_sum(z);
 #pragma unroll
-            for (int j = 0; j < VPT; ++j)
-                if (bi == lane + 32 * j) picked[j] = true;
-        }
+        for (int j = 0; j < VPT; ++j) p[j] = (z > 0.f) ? p[j] / z : 0.f;
     }
-    // softmax over all E logits in fp32, renormalised over the picks
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-        if (lane + 32 * j < E) m = fmaxf(m, v[j]);
-    m = warp_max(m);
-    float p[VPT];
-    float z = 0.f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        p[j] = (lane + 32 * j < E && m > -INFINITY) ? expf(v[j] - m) : 0.f;
-        z += p[j];
-    }
-    z = warp_sum(z);
-    float psel = 0.f;
-#pragma unroll
-    for (int j = 0; j < VPT; ++j) {
-        p[j] = (z > 0.f) ? p[j] / z : 0.f;
-        if (picked[j] && lane + 32 * j < E) psel += p[j];
-    }
-    psel = warp_sum(psel);
     // write the picks in ascending expert id: (j, lane) order
     int base = 0;
     const unsigned lt = lanemask_lt();
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
-        const bool mine = picked[j] && (lane + 32 * j < E);
-        const unsigned b = __ballot_sync(0xffffffffu, mine);
-        if (mine) {
+        const unsigned b = __ballot_sync(0xffffffffu, picked[j]);
+        if (picked[j]) {
             const int pos = base + __popc(b & lt);
             if (pos < k) {
                 ids[pos] = lane + 32 * j;
-                // denominator guard: a row with no finite logit spreads the weight evenly
-                const float wr = renorm ? ((psel > 0.f) ? p[j] / psel : 1.f / k) : p[j];
-                w[pos] = wr * scale;
+                w[pos] = p[j] * scale;
             }
         }
         base += __popc(b);
