@@ -20,12 +20,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int H, float* __restrict__ y) {
     pdl_wait();
     pdl_trigger();
+    // T * H / 4 < 2^31 for every supported shape (checked by the launcher): 32-bit index math
     const int H4 = H / 4;
-    const long total = static_cast<long>(T) * H4;
-    for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<long>(gridDim.x) * blockDim.x) {
-        const int t = static_cast<int>(i / H4);
-        const int n4 = static_cast<int>(i % H4);
+    const int total = T * H4;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int t = i / H4;
+        const int n4 = i - t * H4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (shared) acc = __ldg(reinterpret_cast<const float4*>(shared + static_cast<size_t>(t) * H) + n4);
         for (int j = 0; j < k; ++j) {
@@ -57,6 +57,7 @@ cudaError_t launch_combine(const float* rows, const int32_t* inv, const float* t
                            cudaStream_t st) {
     if (T == 0) return cudaSuccess;
     const long total = static_cast<long>(T) * (H / 4);
+    if (total >= (1L << 31)) return cudaErrorInvalidValue;
     long blocks = (total + 255) / 256;
     if (blocks > 152L * 16) blocks = 152L * 16;
     KernelScope ks_("combine", st);

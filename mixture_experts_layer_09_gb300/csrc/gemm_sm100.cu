@@ -676,32 +676,52 @@ __global__ void __launch_bounds__(256) build_tiles_kernel(const int32_t* __restr
 }
 
 // x16[r] = fp16(x[perm[r] / k]) for the T*k dispatched rows, then x16[T*k + t] = fp16(x[t]);
-// each group of 8 columns is stored in the K order of the dequantised weight tiles.
+// each group of 8 columns is stored in the K order of the dequantised weight tiles.  One warp
+// per row: lane l takes the 16-byte pieces l, l + 32, ..., four loads in flight before the
+// stores.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t* __restrict__ x,
                                                           const int32_t* __restrict__ perm, int T, int k, int H,
                                                           int with_tokens, uint16_t* __restrict__ x16) {
     pdl_wait();
     pdl_trigger();
+    const int lane = threadIdx.x & 31;
     const int n_rows = T * k + (with_tokens ? T : 0);
     const int H8 = H / 8;
-    const long total = static_cast<long>(n_rows) * H8;
-    for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += static_cast<long>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(i / H8), c = static_cast<int>(i % H8);
-        const int t = (r < T * k) ? __ldg(perm + r) / k : r - T * k;
-        const uint4 v = ldg_nc(x + static_cast<size_t>(t) * H + c * 8);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint16_t h[8];  // columns 0..7 as fp16
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            h[2 * j] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] << 16)));
-            h[2 * j + 1] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] & 0xffff0000u)));
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows; r += nw) {
+        int t = r - T * k;
+        if (r < T * k) {
+            int a = 0;
+            if (lane == 0) a = __ldg(perm + r);
+            t = __shfl_sync(0xffffffffu, a, 0) / k;
         }
-        // stored in the GEMM's K order [c0 c4 c1 c5 c2 c6 c3 c7]
-        uint32_t out[4];
+        const uint16_t* src = x + static_cast<size_t>(t) * H;
+        uint4* dst = reinterpret_cast<uint4*>(x16 + static_cast<size_t>(r) * H);
+        for (int c0 = 0; c0 < H8; c0 += 4 * 32) {
+            uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) out[j] = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 4]) << 16);
-        reinterpret_cast<uint4*>(x16 + static_cast<size_t>(r) * H)[c] = make_uint4(out[0], out[1], out[2], out[3]);
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c < H8) v[u] = ldg_nc(src + static_cast<size_t>(c) * 8);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + u * 32 + lane;
+                if (c >= H8) break;
+                const uint32_t in[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint16_t h[8];  // columns 0..7 as fp16
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    h[2 * j] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] << 16)));
+                    h[2 * j + 1] = __half_as_ushort(__float2half_rn(__uint_as_float(in[j] & 0xffff0000u)));
+                }
+                // stored in the GEMM's K order [c0 c4 c1 c5 c2 c6 c3 c7]
+                uint32_t out[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) out[j] = static_cast<uint32_t>(h[j]) | (static_cast<uint32_t>(h[j + 4]) << 16);
+                dst[c] = make_uint4(out[0], out[1], out[2], out[3]);
+            }
+        }
     }
 }
 
@@ -753,9 +773,9 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
     if ((err = set_smem_attrs()) != cudaSuccess) return err;
     // 1. activations in dispatch order (and token order for the shared expert), fp16
     {
-        const long total = static_cast<long>(n_slots + (has_sh ? p.T : 0)) * (p.H / 8);
-        long blocks = (total + 255) / 256;
-        if (blocks > 152L * 8) blocks = 152L * 8;
+        const long rows = n_slots + (has_sh ? p.T : 0);  // one warp per row, 8 per block
+        long blocks = (rows + 7) / 8;
+        if (blocks > static_cast<long>(sm_count()) * 8) blocks = static_cast<long>(sm_count()) * 8;
         if (blocks < 1) blocks = 1;
         {
             KernelScope ks_("gather_rows", st);
