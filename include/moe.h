@@ -196,7 +196,7 @@ MOE_API int moe_dispatch(const int32_t* topk_ids, int T, int k, int E, int32_t* 
  * serving runtime's plugin callback that is not allowed to allocate, or a latency-bound
  * loop that cannot afford the device synchronisation an allocation implies.  This variant
  * runs the same kernels as moe_dispatch with their scratch in one array compiled into the
- * library (about 514 KiB, held on every GPU that loads the library until the process
+ * library (about 66 KiB, held on every GPU that loads the library until the process
  * exits), and allocates nothing.
  *   Arguments and outputs are those of moe_dispatch; T*k must not exceed
  *   MOE_DISPATCH_STATIC_MAX_SLOTS (else MOE_ERR_INVALID_ARG, nothing enqueued).

@@ -9,7 +9,10 @@
 // stable and identical on every run.
 //
 // Small batches (T*k <= kSmallSlots) run one CTA that does all three phases.  Larger ones
-// run count -> scan -> scatter, with per-CTA counts in the workspace.
+// run count -> scatter with per-CTA counts in the workspace; each scatter CTA derives its own
+// starting positions from the whole count table (column totals, their exclusive scan over the
+// experts, and the sum over the CTAs before it), so no scan launch sits between the two.  A
+// CTA takes as few slots as keeps the table (CTAs x E) within 16384 entries and 256 rows.
 //
 // Besides offsets/perm/inv the dispatch writes the list of experts that received at least
 // one slot (ascending) and its length; the expert kernels iterate over that list.
@@ -19,10 +22,20 @@
 
 namespace moe {
 
-constexpr int kSmallSlots = 8192;
-constexpr int kBigWarps = 8;          // warps per CTA in the multi-CTA path
-constexpr int kBigSlotsPerWarp = 256;  // slots per warp in the multi-CTA path
-constexpr int kBigSlotsPerCta = kBigWarps * kBigSlotsPerWarp;
+constexpr int kSmallSlots = 2048;
+constexpr int kBigWarps = 8;            // warps per CTA in the multi-CTA path
+constexpr int kMinSlotsPerCta = 256;    // one 32-slot walk per warp
+constexpr int kMaxTableRows = 256;      // CTAs of the multi-CTA path
+constexpr int kMaxTableInts = 16384;    // count table entries (every scatter CTA reads it whole)
+
+// Slots per CTA of the multi-CTA path: the smallest power-of-two multiple of 256 whose CTA
+// count n / spc fits both the table bounds.
+__host__ __device__ inline int slots_per_cta(int n, int E) {
+    const int max_rows = min(kMaxTableRows, kMaxTableInts / E);
+    int spc = kMinSlotsPerCta;
+    while ((n + spc - 1) / spc > max_rows) spc *= 2;
+    return spc;
+}
 
 // One CTA of 1024 threads (32 warps) for T*k <= kSmallSlots.
 __global__ void __launch_bounds__(1024) dispatch_small_kernel(
@@ -46,15 +59,16 @@ __global__ void __launch_bounds__(1024) dispatch_small_kernel(
 
 // Multi-CTA path, phase 1: per-CTA histogram.
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
-    const int32_t* __restrict__ ids, int n, int E, int* __restrict__ cta_cnt, int* status) {
+    const int32_t* __restrict__ ids, int n, int E, int spc, int* __restrict__ cta_cnt, int* status) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int hist[];  // [kBigWarps][E]
     const int w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kBigWarps * E; i += blockDim.x) hist[i] = 0;
     __syncthreads();
-    const int begin = min(n, blockIdx.x * kBigSlotsPerCta + w * kBigSlotsPerWarp);
-    const int end = min(n, begin + kBigSlotsPerWarp);
+    const int spw = spc / kBigWarps;
+    const int begin = min(n, blockIdx.x * spc + w * spw);
+    const int end = min(n, begin + spw);
     warp_walk(ids, begin, end, E, hist + w * E, 0, nullptr, nullptr, status);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -64,32 +78,61 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
     }
 }
 
-// Phase 2: one CTA (256 threads) turns the per-CTA counts into starting positions.
-__global__ void __launch_bounds__(256) dispatch_scan_kernel(int* cta_cnt, int nblk, int E, int n,
-                                                            int32_t* counts, int32_t* offsets,
-                                                            int32_t* active, int32_t* n_active) {
-    pdl_wait();
-    pdl_trigger();
-    __shared__ int scratch[9];
-    finalize_plan(cta_cnt, nblk, E, n, counts, offsets, active, n_active, scratch);
-}
-
-// Phase 3: stable scatter.
+// Phase 2: stable scatter.  Thread e (one per expert) reads column e of the count table: the
+// expert's total and the part of it counted by the CTAs before this one; the totals' exclusive
+// scan over the experts gives the bucket offsets, which CTA 0 also writes out with the counts
+// and the active-expert list.
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
-    const int32_t* __restrict__ ids, int n, int E, const int* __restrict__ cta_base, int32_t* perm,
-    int32_t* inv, int* status) {
+    const int32_t* __restrict__ ids, int n, int E, int spc, int nblk, const int* __restrict__ cta_cnt,
+    int32_t* counts, int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm, int32_t* inv,
+    int* status) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int hist[];  // [kBigWarps][E]
+    __shared__ int scratch[9];
+    __shared__ int base_e[MOE_MAX_E];
     const int w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kBigWarps * E; i += blockDim.x) hist[i] = 0;
+    {
+        const int e = threadIdx.x;
+        int total = 0, before = 0;
+        if (e < E) {
+            for (int r0 = 0; r0 < nblk; r0 += 4) {
+                int v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) v[u] = (r0 + u < nblk) ? __ldg(cta_cnt + static_cast<size_t>(r0 + u) * E + e) : 0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    total += v[u];
+                    if (r0 + u < static_cast<int>(blockIdx.x)) before += v[u];
+                }
+            }
+        }
+        int sum, nact;
+        const int off = cta_exclusive_scan_256(e < E ? total : 0, scratch, &sum);
+        const int flag = (e < E && total > 0) ? 1 : 0;
+        const int apos = cta_exclusive_scan_256(flag, scratch, &nact);
+        if (e < E) {
+            base_e[e] = off + before;
+            if (blockIdx.x == 0) {
+                offsets[e] = off;
+                if (counts) counts[e] = total;
+                if (flag) active[apos] = e;
+            }
+        }
+        if (blockIdx.x == 0 && e == 0) {
+            offsets[E] = sum;
+            *n_active = nact;
+        }
+    }
     __syncthreads();
-    const int begin = min(n, blockIdx.x * kBigSlotsPerCta + w * kBigSlotsPerWarp);
-    const int end = min(n, begin + kBigSlotsPerWarp);
+    const int spw = spc / kBigWarps;
+    const int begin = min(n, blockIdx.x * spc + w * spw);
+    const int end = min(n, begin + spw);
     warp_walk(ids, begin, end, E, hist + w * E, 0, nullptr, nullptr, nullptr);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = cta_base[static_cast<size_t>(blockIdx.x) * E + e];
+        int run = base_e[e];
         for (int q = 0; q < kBigWarps; ++q) {
             const int tmp = hist[q * E + e];
             hist[q * E + e] = run;
@@ -102,7 +145,8 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
 
 size_t dispatch_scratch_bytes(int n, int E) {
     if (n <= kSmallSlots) return 0;
-    const size_t nblk = (n + kBigSlotsPerCta - 1) / kBigSlotsPerCta;
+    const int spc = slots_per_cta(n, E);
+    const size_t nblk = (n + spc - 1) / spc;
     return align_up(nblk * E * sizeof(int), kWsAlign);
 }
 
@@ -117,47 +161,40 @@ cudaError_t launch_dispatch(const int32_t* ids, int n, int E, int32_t* counts, i
                               inv, active, n_active, status);
         }
     }
-    const int nblk = (n + kBigSlotsPerCta - 1) / kBigSlotsPerCta;
+    const int spc = slots_per_cta(n, E);
+    const int nblk = (n + spc - 1) / spc;
     int* cnt = static_cast<int*>(scratch);
     const size_t smem = kBigWarps * E * sizeof(int);
     {
         KernelScope ks_("dispatch_count", st);
-        cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, cnt,
-                                   status);
-        if (e != cudaSuccess) return e;
-    }
-    {
-        KernelScope ks_("dispatch_scan", st);
-        cudaError_t e = launch_pdl(dispatch_scan_kernel, dim3(1), dim3(256), 0, st, cnt, nblk, E, n, counts, offsets,
-                                   active, n_active);
+        cudaError_t e = launch_pdl(dispatch_count_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, spc,
+                                   cnt, status);
         if (e != cudaSuccess) return e;
     }
     {
         KernelScope ks_("dispatch_scatter", st);
-        return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E,
-                          static_cast<const int*>(cnt), perm, inv, status);
+        return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, spc, nblk,
+                          static_cast<const int*>(cnt), counts, offsets, active, n_active, perm, inv, status);
     }
 }
 
 }  // namespace moe
 
 // ------------------------------------------------------------------ allocation-free variant
-// moe_dispatch_static: the same three dispatch kernels, with their scratch (status word,
+// moe_dispatch_static: the same dispatch kernels, with their scratch (status word,
 // active-expert list, per-CTA count table) in one fixed array compiled into the library
 // instead of a caller workspace.  It serves callers that must not allocate device memory at
 // call time: code running under a framework whose device pool is fixed at start-up, plugin
 // callbacks of a serving runtime that forbid allocation, or latency-critical loops where an
 // allocation's implicit device synchronisation cannot be paid.  Every GPU that loads the
-// library holds the array (about 514 KiB) until the process exits.
+// library holds the array (about 66 KiB) until the process exits.
 #include <mutex>
 
 namespace moe {
 namespace {
 constexpr size_t kStaticStatusBytes = 256;
 constexpr size_t kStaticActiveBytes = 2048;  // active list: E + 1 <= 257 ints
-constexpr size_t kStaticTableBytes =
-    static_cast<size_t>((MOE_DISPATCH_STATIC_MAX_SLOTS + kBigSlotsPerCta - 1) / kBigSlotsPerCta) * MOE_MAX_E *
-    sizeof(int);
+constexpr size_t kStaticTableBytes = static_cast<size_t>(kMaxTableInts) * sizeof(int);  // nblk * E bound
 constexpr size_t kStaticBytes = kStaticStatusBytes + kStaticActiveBytes + kStaticTableBytes;
 }  // namespace
 }  // namespace moe
