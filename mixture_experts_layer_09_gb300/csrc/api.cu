@@ -39,6 +39,7 @@ struct Routing {
     int32_t* active;
     int32_t* n_active;
     void* disp_scratch;
+    int* route_cnt;  // [CTAs][E]: per-CTA expert counts of the counted top-k (prefill layer)
 };
 
 struct GemvBufs {
@@ -54,6 +55,16 @@ struct GemmBufs {
     float* rows; float* sh_rows;
 };
 
+// Tokens per warp of the counted top-k: the fewest (1, 2, 4, ...) that keep its CTA count (8 warps
+// each) at most 64 -- every scatter CTA reads the whole count table -- and within its bounds.
+int counted_tokens_per_warp(int T, int E) {
+    int tpw = 1;
+    while (tpw < (1 << 20) && ((T + 8 * tpw - 1) / (8 * tpw) > 64 ||
+                               !dispatch_counted_supported((T + 8 * tpw - 1) / (8 * tpw), E)))
+        tpw *= 2;
+    return tpw;
+}
+
 void carve_routing(Carver& c, int T, int E, int k, Routing& r) {
     const size_t n = static_cast<size_t>(T) * k;
     r.logits = c.take<float>(static_cast<size_t>(T) * (E + 1));
@@ -66,6 +77,8 @@ void carve_routing(Carver& c, int T, int E, int k, Routing& r) {
     r.active = c.take<int32_t>(E);
     r.n_active = c.take<int32_t>(1);
     r.disp_scratch = c.take<char>(dispatch_scratch_bytes(static_cast<int>(n), E));
+    const int tpw = counted_tokens_per_warp(T, E);
+    r.route_cnt = c.take<int>(static_cast<size_t>((T + 8 * tpw - 1) / (8 * tpw)) * E);
 }
 
 void carve_gemv(Carver& c, int T, int k, int H, int I, int I_sh, GemvBufs& b) {
@@ -237,7 +250,7 @@ int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
     return launch_down_gemv(p, true, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st) {
+int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st, bool tiles_ready = false) {
     const moe_experts* W = c.W;
     GemmPlan p{};
     p.T = c.T; p.k = c.k; p.E = W->E; p.H = W->H; p.I = W->I;
@@ -256,6 +269,7 @@ int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st) {
         p.sh_down_q = c.sh->down.q; p.sh_down_s = c.sh->down.s;
     }
     p.x = c.x; p.x16 = b.x16; p.h16 = b.h16; p.sh_h16 = b.sh_h16; p.tiles = b.tiles; p.n_tiles = b.n_tiles;
+    p.tiles_ready = tiles_ready ? 1 : 0;
     p.status = c.status;
     const bool rows_mode = c.rows_out != nullptr;
     p.rows_out = c.rows_out;
@@ -463,14 +477,30 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
         }
         return run_gemv(mc, b, true, st);
     }
+    GemmBufs b;
+    carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
+    // prefill routing: the top-k launch also counts each CTA's picks per expert, and the dispatch
+    // is the scatter alone, writing the tile list too (no count, scan or tile launches)
+    {
+        const int tpw = counted_tokens_per_warp(T, W->E);
+        const int rblk = (T + 8 * tpw - 1) / (8 * tpw);
+        if (dispatch_counted_supported(rblk, W->E)) {
+            if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            if (launch_dispatch_counted(ids, T * k, W->E, 8 * tpw * k, rblk, r.route_cnt, r.counts, r.offsets, r.perm,
+                                        r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            return run_gemm(mc, b, st, true);
+        }
+    }
     if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active, r.disp_scratch,
                         status, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    GemmBufs b;
-    carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
     return run_gemm(mc, b, st);
 }
 

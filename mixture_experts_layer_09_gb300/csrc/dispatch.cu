@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     const int32_t* __restrict__ ids, int n, int E, int spc, int nblk, const int* __restrict__ cta_cnt,
     int32_t* counts, int32_t* offsets, int32_t* active, int32_t* n_active, int32_t* perm, int32_t* inv,
-    int* status) {
+    int* status, int* tiles, int* n_tiles) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ int hist[];  // [kBigWarps][E]
@@ -123,6 +123,22 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
         if (blockIdx.x == 0 && e == 0) {
             offsets[E] = sum;
             *n_active = nact;
+        }
+        if (tiles && blockIdx.x == 0) {
+            // the tensor arm's tile list (as build_tiles_kernel): a bucket of c rows takes
+            // ceil(c / kGemmTileN) tiles of equal size
+            const int nt = (e < E) ? (total + kGemmTileN - 1) / kGemmTileN : 0;
+            int ntot;
+            const int tb = cta_exclusive_scan_256(nt, scratch, &ntot);
+            if (e < E) {
+                const int per = nt > 0 ? (total + nt - 1) / nt : 0;
+                for (int j = 0; j < nt; ++j) {
+                    tiles[3 * (tb + j)] = e;
+                    tiles[3 * (tb + j) + 1] = off + j * per;
+                    tiles[3 * (tb + j) + 2] = max(0, min(per, total - j * per));
+                }
+            }
+            if (e == 0) *n_tiles = ntot;
         }
     }
     __syncthreads();
@@ -174,8 +190,22 @@ cudaError_t launch_dispatch(const int32_t* ids, int n, int E, int32_t* counts, i
     {
         KernelScope ks_("dispatch_scatter", st);
         return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, spc, nblk,
-                          static_cast<const int*>(cnt), counts, offsets, active, n_active, perm, inv, status);
+                          static_cast<const int*>(cnt), counts, offsets, active, n_active, perm, inv, status,
+                          static_cast<int*>(nullptr), static_cast<int*>(nullptr));
     }
+}
+
+bool dispatch_counted_supported(int nblk, int E) {
+    return nblk >= 1 && nblk <= kMaxTableRows && static_cast<long>(nblk) * E <= kMaxTableInts;
+}
+
+cudaError_t launch_dispatch_counted(const int32_t* ids, int n, int E, int spc, int nblk, const int* cta_cnt,
+                                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                                    int32_t* n_active, int* status, int* tiles, int* n_tiles, cudaStream_t st) {
+    if (spc % kBigWarps || !dispatch_counted_supported(nblk, E)) return cudaErrorInvalidValue;
+    KernelScope ks_("dispatch_scatter+tiles", st);
+    return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), kBigWarps * E * sizeof(int), st, ids,
+                      n, E, spc, nblk, cta_cnt, counts, offsets, active, n_active, perm, inv, status, tiles, n_tiles);
 }
 
 }  // namespace moe

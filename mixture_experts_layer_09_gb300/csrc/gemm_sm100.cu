@@ -783,8 +783,8 @@ cudaError_t launch_gemm_arm(const GemmPlan& p, bool rows_mode, cudaStream_t st) 
                              p.T, p.k, p.H, has_sh ? 1 : 0, p.x16);
         }
     }
-    // 2. tile schedule
-    {
+    // 2. tile schedule (unless the dispatch wrote it)
+    if (!p.tiles_ready) {
         KernelScope ks_("build_tiles", st);
         if (err == cudaSuccess)
             err = launch_pdl(build_tiles_kernel, dim3(1), dim3(256), 0, st, static_cast<const int32_t*>(p.offsets), p.E,

@@ -58,9 +58,21 @@ inline int act_gld(int K) { return ((K / 32) + 3) & ~3; }
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
                                float* w, cudaStream_t st, const float* bias = nullptr, bool renorm = true,
                                float scale = 1.f);
+// The same top-k (fp32 logits, no variants) with each CTA of 8 * tpw tokens counting its picks
+// per expert into row blockIdx.x of cta_cnt [ceil(T / (8 tpw))][E]: the count table of a
+// dispatch whose CTAs take 8 tpw k slots each (launch_dispatch_counted).
+cudaError_t launch_router_topk_counted(const float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids,
+                                       float* w, int* cta_cnt, cudaStream_t st);
 
 // dispatch.cu
 size_t dispatch_scratch_bytes(int n_slots, int E);
+// The scatter alone, for a count table written by the router (CTA c counted slots [c spc, (c + 1)
+// spc)): offsets, counts, active list, perm and inv, and (tiles != nullptr) the tensor arm's tile
+// list.  Needs dispatch_counted_supported(nblk, E).
+bool dispatch_counted_supported(int nblk, int E);
+cudaError_t launch_dispatch_counted(const int32_t* ids, int n_slots, int E, int spc, int nblk, const int* cta_cnt,
+                                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
+                                    int32_t* n_active, int* status, int* tiles, int* n_tiles, cudaStream_t st);
 cudaError_t launch_dispatch(const int32_t* ids, int n_slots, int E, int32_t* counts, int32_t* offsets,
                             int32_t* perm, int32_t* inv, int32_t* active, int32_t* n_active, void* scratch,
                             int* status, cudaStream_t st);
@@ -169,6 +181,7 @@ struct GemmPlan {
     uint16_t* sh_h16;             // fp16 [T][I_sh]
     int* tiles;                   // [3 * ntile_max] (expert, row start, rows)
     int* n_tiles;
+    int tiles_ready;              // the dispatch already wrote the tile list
     int* status;
     // outputs
     float* rows_out;              // ROWS mode [T*k][H], unweighted, dispatch order

@@ -32,13 +32,14 @@ __device__ __forceinline__ float load_logit<CoherentF32>(const CoherentF32* p) {
 }
 
 // VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
-// One warp selects the top-k of one logit row.  ids/w receive the row's k outputs.
+// One warp selects the top-k of one logit row.  ids/w receive the row's k outputs; hist (shared
+// memory, or null) counts each pick.
 // Variants (bias, renorm, scale): the selection runs over logit + bias[e] (bias fp32 [E] or
 // null), the weights stay the unbiased softmax, renormalised over the picks or not, times scale.
 template <typename Tin, int VPT>
 __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E, int k, int32_t* __restrict__ ids,
                                               float* __restrict__ w, const float* __restrict__ bias = nullptr,
-                                              bool renorm = true, float scale = 1.f) {
+                                              bool renorm = true, float scale = 1.f, int* hist = nullptr) {
     const int lane = threadIdx.x & 31;
     float v[VPT];         // logits: the softmax
     uint32_t key[VPT];    // selection scores (logit + bias) as order-preserving integers; 0 once picked
@@ -126,6 +127,7 @@ __device__ __forceinline__ void topk_warp_row(const Tin* __restrict__ row, int E
             if (pos < k) {
                 ids[pos] = lane + 32 * j;
                 w[pos] = p[j] * scale;
+                if (hist) atomicAdd(hist + lane + 32 * j, 1);  // the CTA's picks per expert (shared memory)
             }
         }
         base += __popc(b);

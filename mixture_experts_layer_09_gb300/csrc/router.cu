@@ -241,6 +241,47 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(const Tin* __rest
                             topk_w + static_cast<size_t>(t) * k, bias, renorm != 0, scale);
 }
 
+// Counted variant (prefill layer): 8 warps of tpw tokens each; the CTA's picks per expert go to
+// row blockIdx.x of the dispatch count table.
+template <int VPT>
+__global__ void __launch_bounds__(256) router_topk_counted_kernel(const float* __restrict__ logits, int ld, int T,
+                                                                  int E, int k, int tpw, int32_t* __restrict__ topk_ids,
+                                                                  float* __restrict__ topk_w, int* __restrict__ cta_cnt) {
+    __shared__ int hist[32 * VPT];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    const int t0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * tpw;
+    for (int t = t0; t < min(T, t0 + tpw); ++t)
+        topk_warp_row<float, VPT>(logits + static_cast<size_t>(t) * ld, E, k, topk_ids + static_cast<size_t>(t) * k,
+                                  topk_w + static_cast<size_t>(t) * k, nullptr, true, 1.f, hist);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cta_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+cudaError_t launch_router_topk_counted(const float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids,
+                                       float* w, int* cta_cnt, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    const int vpt = (E + 31) / 32;
+    const dim3 grid((T + 8 * tpw - 1) / (8 * tpw)), block(256);
+    KernelScope ks_("router_topk+count", st);
+    switch (vpt) {
+#define MOE_TOPKC_CASE(V) \
+    case V: return launch_pdl(router_topk_counted_kernel<V>, grid, block, 0, st, logits, ld, T, E, k, tpw, ids, w, cta_cnt);
+        MOE_TOPKC_CASE(1)
+        MOE_TOPKC_CASE(2)
+        MOE_TOPKC_CASE(3)
+        MOE_TOPKC_CASE(4)
+        MOE_TOPKC_CASE(5)
+        MOE_TOPKC_CASE(6)
+        MOE_TOPKC_CASE(7)
+        MOE_TOPKC_CASE(8)
+#undef MOE_TOPKC_CASE
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename Tin>
 static cudaError_t launch_topk_t(const Tin* logits, int ld, int T, int E, int k, int32_t* ids, float* w,
                                  const float* bias, bool renorm, float scale, cudaStream_t st) {
