@@ -55,19 +55,20 @@ struct GemmBufs {
     float* rows; float* sh_rows;
 };
 
-// Tokens per warp of the counted top-k: the fewest (1, 2, 4, ...) that keep its CTA count (8 warps
-// each) at most 64 -- every scatter CTA reads the whole count table -- and within its bounds.
+// Tokens per warp of the counted top-k: the fewest (1, 2, 4, ...) that keep its CTA count
+// (kCountedWarps warps each) at most 64 -- every scatter CTA reads the whole count table -- and
+// within the table's bounds.
+int counted_ctas(int T, int tpw) { return (T + kCountedWarps * tpw - 1) / (kCountedWarps * tpw); }
 int counted_tokens_per_warp(int T, int E) {
     int tpw = 1;
-    while (tpw < (1 << 20) && ((T + 8 * tpw - 1) / (8 * tpw) > 64 ||
-                               !dispatch_counted_supported((T + 8 * tpw - 1) / (8 * tpw), E)))
+    while (tpw < (1 << 20) && (counted_ctas(T, tpw) > 64 || !dispatch_counted_supported(counted_ctas(T, tpw), E)))
         tpw *= 2;
     return tpw;
 }
 
 void carve_routing(Carver& c, int T, int E, int k, Routing& r) {
     const size_t n = static_cast<size_t>(T) * k;
-    r.logits = c.take<float>(static_cast<size_t>(T) * (E + 1));
+    r.logits = c.take<float>(static_cast<size_t>(T) * (E + 1) * 4);  // up to 4 partial planes (K-split router)
     r.ids = c.take<int32_t>(n);
     r.w = c.take<float>(n);
     r.counts = c.take<int32_t>(E);
@@ -78,7 +79,7 @@ void carve_routing(Carver& c, int T, int E, int k, Routing& r) {
     r.n_active = c.take<int32_t>(1);
     r.disp_scratch = c.take<char>(dispatch_scratch_bytes(static_cast<int>(n), E));
     const int tpw = counted_tokens_per_warp(T, E);
-    r.route_cnt = c.take<int>(static_cast<size_t>((T + 8 * tpw - 1) / (8 * tpw)) * E);
+    r.route_cnt = c.take<int>(static_cast<size_t>(counted_ctas(T, tpw)) * E);
 }
 
 void carve_gemv(Carver& c, int T, int k, int H, int I, int I_sh, GemvBufs& b) {
@@ -483,13 +484,22 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     // is the scatter alone, writing the tile list too (no count, scan or tile launches)
     {
         const int tpw = counted_tokens_per_warp(T, W->E);
-        const int rblk = (T + 8 * tpw - 1) / (8 * tpw);
+        const int rblk = counted_ctas(T, tpw);
         if (dispatch_counted_supported(rblk, W->E)) {
-            if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) != cudaSuccess)
+            // tensor-core logits in up to 4 K ranges (more CTAs issuing copies), summed by the top-k
+            int parts = 1;
+            if (router_tc_supported(x, W_r, g, W->H, W->E)) {
+                parts = router_tc_ksplit(W->H);
+                if (launch_router_logits_tc(x, W_r, g, T, W->H, W->E, r.logits, status, st, parts) != cudaSuccess)
+                    return MOE_ERR_CUDA;
+            } else if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) !=
+                       cudaSuccess) {
                 return MOE_ERR_CUDA;
-            if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st) != cudaSuccess)
+            }
+            if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st, parts) !=
+                cudaSuccess)
                 return MOE_ERR_CUDA;
-            if (launch_dispatch_counted(ids, T * k, W->E, 8 * tpw * k, rblk, r.route_cnt, r.counts, r.offsets, r.perm,
+            if (launch_dispatch_counted(ids, T * k, W->E, kCountedWarps * tpw * k, rblk, r.route_cnt, r.counts, r.offsets, r.perm,
                                         r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
                 return MOE_ERR_CUDA;
             return run_gemm(mc, b, st, true);

@@ -50,19 +50,26 @@ cudaError_t launch_router_logits(const uint16_t* x, const uint16_t* W_r, const u
 // router_tc.cu: tcgen05 logits GEMM for T > 32 (status: device timeout record, may be null)
 // (H % 64 == 0, 1 <= E <= 256, x / W_r / g 16-byte aligned)
 bool router_tc_supported(const void* x, const void* W_r, const void* g, int H, int E);
+// ksplit > 1: partial logits of ksplit equal K ranges in planes T * (E + (g != 0)) floats apart
+// (router_tc_ksplit(H) picks up to 4 ranges of at least 4 K-steps); the planes sum to the logits.
+int router_tc_ksplit(int H);
 cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H, int E,
-                                    float* logits, int* status, cudaStream_t st);
+                                    float* logits, int* status, cudaStream_t st, int ksplit = 1);
 // group row stride of the quantised activations: K/32 rounded up to a multiple of 4
 inline int act_gld(int K) { return ((K / 32) + 3) & ~3; }
 // bias (fp32 [E], selection only), renorm, scale: the router variants (defaults: plain softmax top-k)
 cudaError_t launch_router_topk(const void* logits, bool is_bf16, int ld, int T, int E, int k, int32_t* ids,
                                float* w, cudaStream_t st, const float* bias = nullptr, bool renorm = true,
                                float scale = 1.f);
-// The same top-k (fp32 logits, no variants) with each CTA of 8 * tpw tokens counting its picks
-// per expert into row blockIdx.x of cta_cnt [ceil(T / (8 tpw))][E]: the count table of a
-// dispatch whose CTAs take 8 tpw k slots each (launch_dispatch_counted).
-cudaError_t launch_router_topk_counted(const float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids,
-                                       float* w, int* cta_cnt, cudaStream_t st);
+// The same top-k (fp32 logits, no variants) with each CTA of kCountedWarps * tpw tokens counting
+// its picks per expert into row blockIdx.x of cta_cnt [ceil(T / (kCountedWarps tpw))][E]: the
+// count table of a dispatch whose CTAs take kCountedWarps tpw k slots each
+// (launch_dispatch_counted).
+constexpr int kCountedWarps = 16;
+// parts > 1: the logits arrive as `parts` partial planes (T * ld floats apart, plane 0 at `logits`);
+// each warp sums them in plane order into plane 0 (the final logits) before its top-k.
+cudaError_t launch_router_topk_counted(float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids, float* w,
+                                       int* cta_cnt, cudaStream_t st, int parts = 1);
 
 // dispatch.cu
 size_t dispatch_scratch_bytes(int n_slots, int E);

@@ -241,34 +241,63 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(const Tin* __rest
                             topk_w + static_cast<size_t>(t) * k, bias, renorm != 0, scale);
 }
 
-// Counted variant (prefill layer): 8 warps of tpw tokens each; the CTA's picks per expert go to
-// row blockIdx.x of the dispatch count table.
+// Counted variant (prefill layer): kCountedWarps warps of tpw tokens each; the CTA's picks per
+// expert go to row blockIdx.x of the dispatch count table.
 template <int VPT>
-__global__ void __launch_bounds__(256) router_topk_counted_kernel(const float* __restrict__ logits, int ld, int T,
-                                                                  int E, int k, int tpw, int32_t* __restrict__ topk_ids,
-                                                                  float* __restrict__ topk_w, int* __restrict__ cta_cnt) {
+__global__ void __launch_bounds__(kCountedWarps * 32) router_topk_counted_kernel(float* logits, int ld, int T, int E, int k, int tpw,
+                                                                  int32_t* __restrict__ topk_ids,
+                                                                  float* __restrict__ topk_w, int* __restrict__ cta_cnt,
+                                                                  int parts) {
     __shared__ int hist[32 * VPT];
     for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    const int t0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * tpw;
-    for (int t = t0; t < min(T, t0 + tpw); ++t)
-        topk_warp_row<float, VPT>(logits + static_cast<size_t>(t) * ld, E, k, topk_ids + static_cast<size_t>(t) * k,
-                                  topk_w + static_cast<size_t>(t) * k, nullptr, true, 1.f, hist);
+    const int c0 = blockIdx.x * (blockDim.x >> 5) * tpw;  // the CTA's first token
+    if (parts > 1) {
+        // the final logits (the shared gate included): the CTA's rows of the partial planes summed
+        // in plane order into plane 0, every thread several values with all their loads in flight
+        const size_t plane = static_cast<size_t>(T) * ld;
+        const int nval = (min(T, c0 + static_cast<int>(blockDim.x >> 5) * tpw) - c0) * ld;
+        float* base = logits + static_cast<size_t>(c0) * ld;
+        for (int i = threadIdx.x; i < nval; i += blockDim.x) {
+            float v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = (q < parts) ? __ldg(base + q * plane + i) : 0.f;
+            float sum = v[0];
+#pragma unroll
+            for (int q = 1; q < 4; ++q)
+                if (q < parts) sum += v[q];
+            base[i] = sum;
+        }
+        __syncthreads();
+    }
+    const int t0 = c0 + (threadIdx.x >> 5) * tpw;
+    for (int t = t0; t < min(T, t0 + tpw); ++t) {
+        const float* row = logits + static_cast<size_t>(t) * ld;
+        if (parts > 1)
+            topk_warp_row<CoherentF32, VPT>(reinterpret_cast<const CoherentF32*>(row), E, k,
+                                            topk_ids + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k,
+                                            nullptr, true, 1.f, hist);
+        else
+            topk_warp_row<float, VPT>(row, E, k, topk_ids + static_cast<size_t>(t) * k,
+                                      topk_w + static_cast<size_t>(t) * k, nullptr, true, 1.f, hist);
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) cta_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-cudaError_t launch_router_topk_counted(const float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids,
-                                       float* w, int* cta_cnt, cudaStream_t st) {
+cudaError_t launch_router_topk_counted(float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids, float* w,
+                                       int* cta_cnt, cudaStream_t st, int parts) {
     if (T == 0) return cudaSuccess;
     const int vpt = (E + 31) / 32;
-    const dim3 grid((T + 8 * tpw - 1) / (8 * tpw)), block(256);
+    const dim3 grid((T + kCountedWarps * tpw - 1) / (kCountedWarps * tpw)), block(kCountedWarps * 32);
     KernelScope ks_("router_topk+count", st);
     switch (vpt) {
 #define MOE_TOPKC_CASE(V) \
-    case V: return launch_pdl(router_topk_counted_kernel<V>, grid, block, 0, st, logits, ld, T, E, k, tpw, ids, w, cta_cnt);
+    case V:                                                                                                    \
+        return launch_pdl(router_topk_counted_kernel<V>, grid, block, 0, st, logits, ld, T, E, k, tpw, ids, w, \
+                          cta_cnt, parts);
         MOE_TOPKC_CASE(1)
         MOE_TOPKC_CASE(2)
         MOE_TOPKC_CASE(3)

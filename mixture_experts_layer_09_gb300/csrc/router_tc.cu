@@ -7,7 +7,9 @@
 // B in 128-byte-swizzled K-major tiles, fp32 accumulators in tensor memory.  Warp 0 brings the
 // token tile (two boxes) and the router rows by TMA, one copy per lane, and writes the gate row
 // into the B tile itself; warp 1 issues the MMAs; warps 2-5 read the accumulators and store the
-// logits.  Waits are bounded.
+// logits.  Waits are bounded.  With ksplit > 1 (prefill layer) the grid's y index takes one of
+// ksplit equal K ranges and the epilogue writes that range's partial logits to plane y of the
+// output (planes T * ld apart); the consumer sums the planes in order.
 #include <cuda.h>
 
 #include <algorithm>
@@ -34,6 +36,7 @@ struct RouterTcArgs {
     int T, H, E, ld;
     int tile_b;         // bytes of one B tile: round16(E + (g != 0)) rows of 128 bytes
     int stages;         // pipeline depth, 2 .. kMaxStages
+    int ksplit;         // K ranges (grid y); plane y of logits holds range y's partial sums
     float* logits;
     int* status;
 };
@@ -47,7 +50,8 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
     pdl_trigger();
     const int t0 = blockIdx.x * RM;
     const int ncols = p.E + (p.g ? 1 : 0);
-    const int nk = p.H / RK;
+    const int nk = p.H / RK / p.ksplit;          // K-steps of this CTA's range
+    const int kb0 = static_cast<int>(blockIdx.y) * nk;
     const int RS = p.stages;
     const int stage_bytes = kTileA + p.tile_b;
     extern __shared__ uint8_t smem_raw[];
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
             uint8_t* sb = sa + kTileA;
             if (p.g && lane < 8) {
                 // row E of the B tile: 8 chunks of 16 bytes, in the tile's 128-byte swizzle
-                const uint4 v = reinterpret_cast<const uint4*>(gbuf + kb * RK * 2)[lane];
+                const uint4 v = reinterpret_cast<const uint4*>(gbuf + (kb0 + kb) * RK * 2)[lane];
                 *reinterpret_cast<uint4*>(sb + p.E * 128 + ((lane ^ (p.E & 7)) << 4)) = v;
                 fence_proxy_async_smem();
             }
@@ -103,8 +107,9 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
             __syncwarp();
             // the token tile as two 64-row boxes and the router rows, each from its own lane:
             // copies issued by one thread are served one after another
-            if (lane < 2) tma_load_2d(sa + lane * (RM / 2) * 128, &p.tm_x, kb * RK, t0 + lane * (RM / 2), full + s);
-            if (lane == 2) tma_load_2d(sb, &p.tm_w, kb * RK, 0, full + s);
+            if (lane < 2)
+                tma_load_2d(sa + lane * (RM / 2) * 128, &p.tm_x, (kb0 + kb) * RK, t0 + lane * (RM / 2), full + s);
+            if (lane == 2) tma_load_2d(sb, &p.tm_w, (kb0 + kb) * RK, 0, full + s);
             issued = kb + 1;
         }
         if (*abort_flag && lane == 0) {
@@ -160,7 +165,8 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
                 if (t < p.T) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < ncols) p.logits[static_cast<size_t>(t) * p.ld + c0 + j] = v[j];
+                        if (c0 + j < ncols)
+                            p.logits[(static_cast<size_t>(blockIdx.y) * p.T + t) * p.ld + c0 + j] = v[j];
                 }
             }
         }
@@ -178,9 +184,18 @@ bool router_tc_supported(const void* x, const void* W_r, const void* g, int H, i
     return H % RK == 0 && E >= 1 && E <= 256 && aligned(x) && aligned(W_r) && aligned(g);
 }
 
+int router_tc_ksplit(int H) {
+    const int steps = H / RK;
+    for (int s = 4; s > 1; s >>= 1)
+        if (steps % s == 0 && steps / s >= 4) return s;
+    return 1;
+}
+
 cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, const uint16_t* g, int T, int H, int E,
-                                    float* logits, int* status, cudaStream_t st) {
+                                    float* logits, int* status, cudaStream_t st, int ksplit) {
     RouterTcArgs a{};
+    if (ksplit < 1 || (H / RK) % ksplit) return cudaErrorInvalidValue;
+    a.ksplit = ksplit;
     if (!tmap_2d(&a.tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(H), static_cast<uint64_t>(T),
                  static_cast<uint64_t>(H) * 2, RK, RM / 2, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -204,7 +219,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, const uint16_t* W_r, cons
         cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (attr != cudaSuccess) return attr;
     KernelScope ks_("router_logits_tc", st);
-    return launch_pdl(router_logits_tc_kernel, dim3((T + RM - 1) / RM), dim3(192), smem, st, a);
+    return launch_pdl(router_logits_tc_kernel, dim3((T + RM - 1) / RM, ksplit), dim3(192), smem, st, a);
 }
 
 }  // namespace moe
