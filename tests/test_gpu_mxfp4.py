@@ -115,4 +115,7 @@ def test_layer_qwen3_decode_t16_mxfp4(moe):
 
 
 def test_layer_qwen15_prefill_t4096_mxfp4(moe):
+    """MXFP4 routed experts with the int4 shared expert at T=4096, on tokens covering every token
+    tile of every expert (every element passes too, in about 100 s of oracle time on 16 cores;
+    the int4 twin of this layer is compared whole in test_gpu_layer.py)."""
     _check_layer(moe, wk.layer("qwen15_prefill_t4096_mxfp4"), sample="buckets")
