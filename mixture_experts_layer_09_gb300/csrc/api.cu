@@ -480,38 +480,28 @@ int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_
     }
     GemmBufs b;
     carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
-    // prefill routing: the top-k launch also counts each CTA's picks per expert, and the dispatch
-    // is the scatter alone, writing the tile list too (no count, scan or tile launches)
-    {
-        const int tpw = counted_tokens_per_warp(T, W->E);
-        const int rblk = counted_ctas(T, tpw);
-        if (dispatch_counted_supported(rblk, W->E)) {
-            // tensor-core logits in up to 4 K ranges (more CTAs issuing copies), summed by the top-k
-            int parts = 1;
-            if (router_tc_supported(x, W_r, g, W->H, W->E)) {
-                parts = router_tc_ksplit(W->H);
-                if (launch_router_logits_tc(x, W_r, g, T, W->H, W->E, r.logits, status, st, parts) != cudaSuccess)
-                    return MOE_ERR_CUDA;
-            } else if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) !=
-                       cudaSuccess) {
-                return MOE_ERR_CUDA;
-            }
-            if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st, parts) !=
-                cudaSuccess)
-                return MOE_ERR_CUDA;
-            if (launch_dispatch_counted(ids, T * k, W->E, kCountedWarps * tpw * k, rblk, r.route_cnt, r.counts, r.offsets, r.perm,
-                                        r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
-            return run_gemm(mc, b, st, true);
-        }
+    // prefill routing: the top-k launch also counts each CTA's picks per expert (at most 64 CTAs,
+    // so the count table always fits: 64 * E <= 16384 for E <= 256), and the dispatch is the
+    // scatter alone, writing the tile list too (no count, scan or tile launches)
+    const int tpw = counted_tokens_per_warp(T, W->E);
+    const int rblk = counted_ctas(T, tpw);
+    if (!dispatch_counted_supported(rblk, W->E)) return MOE_ERR_UNSUPPORTED;
+    // tensor-core logits in up to 4 K ranges (more CTAs issuing copies), summed by the top-k
+    int parts = 1;
+    if (router_tc_supported(x, W_r, g, W->H, W->E)) {
+        parts = router_tc_ksplit(W->H);
+        if (launch_router_logits_tc(x, W_r, g, T, W->H, W->E, r.logits, status, st, parts) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) !=
+               cudaSuccess) {
+        return MOE_ERR_CUDA;
     }
-    if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) != cudaSuccess)
+    if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st, parts) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active, r.disp_scratch,
-                        status, st) != cudaSuccess)
+    if (launch_dispatch_counted(ids, T * k, W->E, kCountedWarps * tpw * k, rblk, r.route_cnt, r.counts, r.offsets,
+                                r.perm, r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
         return MOE_ERR_CUDA;
-    return run_gemm(mc, b, st);
+    return run_gemm(mc, b, st, true);
 }
 
 int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* y_norm,
