@@ -135,9 +135,13 @@ def _dispatch_gpu(moe, ids_np, E):
     return [t.cpu().numpy() for t in (counts, offsets, perm, inv)], st
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (4, 8, 2), (16, 128, 8), (8, 256, 32), (1024, 64, 8),
-                                   (1023, 60, 4), (2048, 256, 8), (16384, 256, 8), (16384, 32, 8), (8192, 8, 2)])
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (4, 8, 2), (16, 128, 8), (8, 256, 32), (512, 8, 4), (2049, 16, 1),
+                                   (1024, 64, 8), (1023, 60, 4), (2048, 256, 8), (16384, 256, 8), (16384, 32, 8),
+                                   (8192, 8, 2)])
 def test_dispatch_bit_exact(moe, T, E, k):
+    """Both dispatch paths against the oracle: one CTA up to 2048 slots (512 x 4 is the last),
+    count -> scatter above (2049 x 1 leaves one slot to its last CTA), with count tables at
+    their row cap (16384 x 32) and entry cap (2048 x 256 and 16384 x 256)."""
     g = gen.rng(7, T, E, k)
     ids = np.stack([np.sort(g.choice(E, size=k, replace=False)) for _ in range(T)]).astype(np.int32)
     ref = oracle.dispatch(ids, E)
