@@ -395,8 +395,8 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + TB * 2 * 32);
     int* last_flag = const_cast<int*>(abort_flag) + 1;
 
-    pdl_wait();
-    pdl_trigger();
+    // set-up that reads nothing an earlier kernel writes runs before the dependency wait, during
+    // the previous kernel's tail: the stage barriers and the TMA descriptors this mode uses
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -406,7 +406,26 @@ __global__ void __launch_bounds__((kCW + 1) * 32, 2) gemv_pipe_kernel(const __gr
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (warp == kCW && lane == 0) {
+        if (MODE == 0) {
+            prefetch_tmap(&p.tm_gate);
+            prefetch_tmap(&p.tm_up);
+            prefetch_tmap(&p.tm_gate_s);
+            prefetch_tmap(&p.tm_up_s);
+            prefetch_tmap(&p.tm_sh_gate);
+            prefetch_tmap(&p.tm_sh_up);
+            prefetch_tmap(&p.tm_sh_gate_s);
+            prefetch_tmap(&p.tm_sh_up_s);
+        } else {
+            prefetch_tmap(&p.tm_down);
+            prefetch_tmap(&p.tm_down_s);
+            prefetch_tmap(&p.tm_sh_down);
+            prefetch_tmap(&p.tm_sh_down_s);
+        }
+    }
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == kCW) {
         // ---------------- producer
