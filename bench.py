@@ -11,6 +11,10 @@ cycling 2 independent layer replicas (311 MB of experts each, far above the 129 
 distinct token batches.  Each step is timed by its own CUDA-event pair on the launching stream
 (the median and the 10th / 90th percentiles are reported beside the whole region's mean).
 
+``e2e`` is the same layer called from pinned host buffers (inputs in, y out, every step), the
+copies overlapped with the neighbouring steps' layers on their own streams; its ``serial_value``
+is the same loop on one stream.
+
 The line also carries, as flat numbers in ``config``, the decode layers (Qwen3-30B-A3B-shaped
 T=1/4/16 and GLM-class k=8/32 T=1/8, bound by HBM), the T=512 prefill layer, the router +
 dispatch sweep and the skewed tiny layer; the fp64 CPU oracle is timed on the host cores, all
@@ -195,6 +199,87 @@ def timed_steps(torch, fn, steps, warmup, dist=None):
     per = [1e3 * ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
     total = ev[0].elapsed_time(ev[steps]) / 1e3
     return reduce_max(dist, total, "cuda"), per
+
+
+def pipelined_e2e(torch, layers, xd, rd, T, H, steps, warmup, dist=None):
+    """End-to-end step loop through pinned host buffers (x and the residual in, y out, every
+    step), copies overlapped with the neighbouring steps' layers: a copy-in stream, the compute
+    stream and a copy-out stream, two device buffers of each, events for the hand-offs.  The
+    region runs from a synchronized start to the last output copy's completion; returns total
+    seconds (max over ranks)."""
+    n_in = len(xd)
+    xh = [t.cpu().pin_memory() for t in xd]
+    rh = [t.cpu().pin_memory() for t in rd]
+    yh = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in range(2)]
+    xin = [torch.empty((T, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    rin = [torch.empty((T, H), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    yd = [torch.empty((T, H), dtype=torch.float32, device="cuda") for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_cmp = torch.cuda.current_stream()
+
+    def run(n0, n):
+        ev_in = {}   # inputs of step i on the device
+        ev_cmp = {}  # layer of step i done (its inputs free, its y ready)
+        ev_out = {}  # y of step i copied out
+        for j in range(n):
+            i = n0 + j
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if j >= 2:
+                    s_in.wait_event(ev_cmp[i - 2])  # the buffer's previous layer has read it
+                xin[b].copy_(xh[i % n_in], non_blocking=True)
+                rin[b].copy_(rh[i % n_in], non_blocking=True)
+                ev_in[i] = torch.cuda.Event()
+                ev_in[i].record(s_in)
+            s_cmp.wait_event(ev_in[i])
+            if j >= 2:
+                s_cmp.wait_event(ev_out[i - 2])  # the buffer's previous y has been copied out
+            layers[i % len(layers)].forward(xin[b], rin[b], y=yd[b])
+            ev_cmp[i] = torch.cuda.Event()
+            ev_cmp[i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[i])
+                yh[b].copy_(yd[b], non_blocking=True)
+                ev_out[i] = torch.cuda.Event()
+                ev_out[i].record(s_out)
+        s_cmp.wait_stream(s_in)
+        s_cmp.wait_stream(s_out)
+
+    run(0, warmup)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_cmp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    run(warmup, steps)
+    e1.record(s_cmp)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return reduce_max(dist, e0.elapsed_time(e1) / 1e3, "cuda")
+
+
+def serial_e2e(torch, layers, xd, rd, T, H, steps, warmup, dist=None):
+    """The end-to-end step on one stream: copy x and the residual in, the layer, copy y out."""
+    n_in = len(xd)
+    xh = [t.cpu().pin_memory() for t in xd]
+    rh = [t.cpu().pin_memory() for t in rd]
+    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    xin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    rin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    yd = torch.empty((T, H), dtype=torch.float32, device="cuda")
+
+    def step(i):
+        xin.copy_(xh[i % n_in], non_blocking=True)
+        rin.copy_(rh[i % n_in], non_blocking=True)
+        layers[i % len(layers)].forward(xin, rin, y=yd)
+        yh.copy_(yd, non_blocking=True)
+
+    total, _ = timed_steps(torch, step, steps, warmup, dist)
+    return total
 
 
 def summary(per_us):
@@ -587,20 +672,13 @@ def run_ours(args, rank, world):
     graph = summary(perg)
     kern = kernel_times(torch, moe, step, args.steps)
 
-    # end to end through host buffers: H2D of x and the residual, the layer, D2H of y, every step
-    xh = [t.cpu().pin_memory() for t in xd]
-    rh = [t.cpu().pin_memory() for t in rd]
-    yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
-    xin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-    rin = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
-
-    def e2e_step(i):
-        xin.copy_(xh[i % N_PREFILL_INPUTS], non_blocking=True)
-        rin.copy_(rh[i % N_PREFILL_INPUTS], non_blocking=True)
-        layers[i % N_PREFILL_REPLICAS].forward(xin, rin, y=y)
-        yh.copy_(y, non_blocking=True)
-
-    e2e_s, _ = timed_steps(torch, e2e_step, args.steps, args.warmup, dist)
+    # end to end through host buffers: every step copies its x and residual in from pinned host
+    # memory, runs the layer and copies y out, as a serving loop would: on three streams, step
+    # i + 1's input copies and step i - 1's output copy overlap step i's layer (double-buffered
+    # device inputs and outputs, ordered by events)
+    e2e_s = pipelined_e2e(torch, layers, xd, rd, T, H, args.steps, args.warmup, dist)
+    # the same without the overlap (one stream: copy in, layer, copy out), reported beside it
+    e2e_serial_s = serial_e2e(torch, layers, xd, rd, T, H, args.steps, args.warmup, dist)
     del layers, xd, rd
     torch.cuda.empty_cache()
 
@@ -687,7 +765,9 @@ def run_ours(args, rank, world):
         "gpu_launches": int(round(launches)),
         "clocks": clk,
         "e2e": {"value": job_value(world, T, args.steps, e2e_s), "unit": "tokens/s",
-                "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": T * H * 4},
+                "h2d_bytes_per_step": 2 * T * H * 2, "d2h_bytes_per_step": T * H * 4,
+                "copies": "each step's input and output copies overlap the neighbouring steps' layers (3 streams)",
+                "serial_value": job_value(world, T, args.steps, e2e_serial_s)},
         **extra,
     }
     if not args.no_cpu_baseline:
