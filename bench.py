@@ -415,26 +415,42 @@ def measure_decode(torch, moe, args, seed0):
 
 
 def measure_norm(torch, moe, args, seed0):
-    """The T=16 decode layer with its RMSNorm output (moe_layer_forward_norm)."""
+    """The layer with its RMSNorm output (moe_layer_forward_norm) beside the plain layer call,
+    on the T=1 and T=16 decode layers (GEMV arm: the norm is one more launch) and the T=4096
+    prefill layer (tensor arm: the combine norms its rows)."""
     from mixture_experts_layer_09_gb300.run_case import upload
-    D = DECODE
-    H, T = D["H"], 16
-    layers = [upload(torch, moe, gen.Workload("d", T, H, D["I"], D["E"], D["k"]), seed0 + rep)
-              for rep in range(N_DECODE_REPLICAS)]
-    gamma = torch.from_numpy(gen.bf16_bits(gen.rng(23, H).normal(1.0, 0.1, size=H).astype(np.float32))
-                             .view(np.int16)).view(torch.bfloat16).cuda()
-    xs = [_to_dev(torch, gen.draw_x(1500 + i, T, H)) for i in range(N_DECODE_INPUTS)]
-    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
-    yn = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    out = {}
+    D, P = DECODE, HEADLINE
+    cases = [("decode_t1", gen.Workload("d", 1, D["H"], D["I"], D["E"], D["k"]), N_DECODE_REPLICAS,
+              N_DECODE_INPUTS, 1500),
+             ("decode_t16", gen.Workload("d", 16, D["H"], D["I"], D["E"], D["k"]), N_DECODE_REPLICAS,
+              N_DECODE_INPUTS, 1500),
+             ("prefill_t4096", gen.Workload("pn", 4096, P["H"], P["I"], P["E"], P["k"], I_sh=P["I_sh"]),
+              N_PREFILL_REPLICAS, N_PREFILL_INPUTS, 1700)]
+    for name, wl, n_rep, n_in, xseed in cases:
+        H, T = wl.H, wl.T
+        layers = [upload(torch, moe, wl, seed0 + 80 + rep) for rep in range(n_rep)]
+        gamma = torch.from_numpy(gen.bf16_bits(gen.rng(23, H).normal(1.0, 0.1, size=H).astype(np.float32))
+                                 .view(np.int16)).view(torch.bfloat16).cuda()
+        xs = [_to_dev(torch, gen.draw_x(xseed + i, T, H)) for i in range(n_in)]
+        y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+        yn = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
 
-    def step(i):
-        layers[i % len(layers)].forward(xs[i % N_DECODE_INPUTS], None, y=y, norm_gamma=gamma, eps=1e-6, y_norm=yn)
+        def step_norm(i):
+            layers[i % n_rep].forward(xs[i % n_in], None, y=y, norm_gamma=gamma, eps=1e-6, y_norm=yn)
 
-    _, per = timed_steps(torch, step, max(50, args.steps), args.warmup)
-    del layers
-    torch.cuda.empty_cache()
-    us = summary(per)["median_us"]
-    return {"us_per_layer_with_rmsnorm": us, "tokens_per_s": T / (us * 1e-6)}
+        def step_plain(i):
+            layers[i % n_rep].forward(xs[i % n_in], None, y=y)
+
+        steps = max(50, args.steps)
+        _, per_n = timed_steps(torch, step_norm, steps, args.warmup)
+        _, per_p = timed_steps(torch, step_plain, steps, args.warmup)
+        del layers
+        torch.cuda.empty_cache()
+        us_n, us_p = summary(per_n)["median_us"], summary(per_p)["median_us"]
+        out[name] = {"us_per_layer_with_rmsnorm": us_n, "us_per_layer_plain": us_p,
+                     "tokens_per_s_with_rmsnorm": T / (us_n * 1e-6)}
+    return out
 
 
 def measure_glm(torch, moe, args):
@@ -688,7 +704,7 @@ def run_ours(args, rank, world):
         extra["decode"] = measure_decode(torch, moe, args, seed0)
         extra["decode_glm"] = measure_glm(torch, moe, args)
         extra["prefill_t512"] = measure_prefill_t512(torch, moe, args, seed0)
-        extra["decode_with_rmsnorm"] = measure_norm(torch, moe, args, seed0)
+        extra["with_rmsnorm"] = measure_norm(torch, moe, args, seed0)
         extra["router_dispatch_sweep"] = measure_router_sweep(torch, moe, args)
         extra["skewed_layer"] = measure_skewed_layer(torch, moe, args)
         extra["mxfp4"] = measure_mxfp4(torch, moe, args)

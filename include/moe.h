@@ -253,8 +253,11 @@ MOE_API int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const
 MOE_API int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* y_norm,
                         moe_stream_t stream);
 
-/* moe_layer_forward followed by moe_rmsnorm of its y (one more launch on the same stream):
- * y receives the layer output, y_norm its RMSNorm with norm_gamma bf16 [H] and eps. */
+/* moe_layer_forward with the RMSNorm of its y: y receives the layer output, y_norm its RMSNorm
+ * with norm_gamma bf16 [H] and eps, bit-identical to moe_rmsnorm on that y.  The tensor arm's
+ * combine norms each row as it writes it (no extra launch, no second read of y); the GEMV arm,
+ * whose combine is folded into the down projection, runs the norm as one more launch on the
+ * same stream. */
 MOE_API int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r,
                                    const moe_experts* W, const moe_shared* sh, int T, int k, float* y,
                                    const uint16_t* norm_gamma, float eps, uint16_t* y_norm,

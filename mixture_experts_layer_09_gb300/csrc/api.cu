@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "norm.h"
 #include "quant.cuh"
 
 using namespace moe;
@@ -205,6 +206,7 @@ struct MlpCall {
     float* rows_out;      // rows mode target (moe_expert_mlp) or nullptr
     float* y;             // layer mode target
     int* status;
+    const NormOut* norm;  // layer mode: RMSNorm of y too, or nullptr
 };
 
 int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
@@ -248,7 +250,9 @@ int run_gemv(const MlpCall& c, GemvBufs& b, bool x_quantized, cudaStream_t st) {
     p.col_counter = reinterpret_cast<int*>(reinterpret_cast<char*>(c.status) + kWsCounterOffset);
     p.residual = c.residual;
     p.y = c.y;
-    return launch_down_gemv(p, true, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (launch_down_gemv(p, true, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!c.norm) return MOE_OK;
+    return status_of(launch_rmsnorm(c.y, c.norm->gamma, c.T, W->H, c.norm->eps, c.norm->y_norm, st));
 }
 
 int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st, bool tiles_ready = false) {
@@ -278,11 +282,96 @@ int run_gemm(const MlpCall& c, GemmBufs& b, cudaStream_t st, bool tiles_ready = 
     p.sh_out = b.sh_rows;
     if (launch_gemm_arm(p, rows_mode, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (!rows_mode) {
-        if (launch_combine(b.rows, c.inv, c.topk_w, true, c.sh ? b.sh_rows : nullptr, c.residual, c.T, c.k, W->H,
-                           c.y, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        const float* shr = c.sh ? b.sh_rows : nullptr;
+        const cudaError_t e =
+            c.norm ? launch_combine_norm(b.rows, c.inv, c.topk_w, true, shr, c.residual, c.T, c.k, W->H, c.y, *c.norm, st)
+                   : launch_combine(b.rows, c.inv, c.topk_w, true, shr, c.residual, c.T, c.k, W->H, c.y, st);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
     return MOE_OK;
+}
+
+// The layer call, with the RMSNorm of its output when `norm` is set: the tensor arm's combine
+// norms each row as it writes it.  On the GEMV arm the combine is folded into the down
+// projection, whose column blocks finish in no fixed order; a row is complete only when the
+// last block is, and one CTA norming every row then was slower than the norm's own launch
+// (one CTA per row on as many SMs), so the norm follows as that launch.
+int layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r, const moe_experts* W,
+                  const moe_shared* sh, int T, int k, float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
+                  void* ws, size_t ws_bytes, moe_stream_t stream, const NormOut* norm) {
+    if (int s = check_experts(W)) return s;
+    if (int s = check_shared(sh)) return s;
+    if (T < 0 || k < 1 || k > MOE_MAX_K || k > W->E) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !W_r || !y || !ws || !aligned16(x) || !aligned16(W_r) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+    if (residual && (reinterpret_cast<uintptr_t>(residual) & 7u)) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
+    const int I_sh = sh ? sh->I_sh : 0;
+    if (ws_bytes < moe_workspace_size(T, W->E, k, W->H, W->I, I_sh)) return MOE_ERR_INVALID_ARG;
+    const int a = choose_arm(arm, T, k, W->E, W->H, W->I, I_sh);
+    if (a < 0) return arm == MOE_ARM_AUTO || arm == MOE_ARM_GEMV || arm == MOE_ARM_GEMM ? MOE_ERR_UNSUPPORTED
+                                                                                      : MOE_ERR_INVALID_ARG;
+    if (int s = check_device()) return s;
+    cudaStream_t st = S(stream);
+    int* status = static_cast<int*>(ws);
+    Carver c(ws);
+    Routing r;
+    carve_routing(c, T, W->E, k, r);
+    int32_t* ids = topk_ids_out ? topk_ids_out : r.ids;
+    float* w = topk_w_out ? topk_w_out : r.w;
+    const uint16_t* g = sh ? sh->g : nullptr;
+    const int ld = W->E + (g ? 1 : 0);
+    MlpCall mc{};
+    mc.x = x; mc.T = T; mc.k = k; mc.W = W; mc.sh = sh; mc.logits = r.logits; mc.logit_ld = ld;
+    mc.offsets = r.offsets; mc.perm = r.perm; mc.inv = r.inv; mc.active = r.active; mc.n_active = r.n_active;
+    mc.topk_w = w; mc.residual = residual; mc.rows_out = nullptr; mc.y = y; mc.status = status;
+    mc.norm = norm;
+    if (a == MOE_ARM_GEMV) {
+        GemvBufs b;
+        carve_gemv(c, T, k, W->H, W->I, I_sh, b);
+        // decode batches: 3 launches -- logits + x quantisation + top-k + dispatch, gate/up, down + combine
+        const bool fused_routing = T <= 32;
+        DecodeRoute dr;
+        if (fused_routing) {
+            dr.k = k; dr.ids = ids; dr.w = w; dr.counts = r.counts; dr.offsets = r.offsets; dr.perm = r.perm;
+            dr.inv = r.inv; dr.active = r.active; dr.n_active = r.n_active; dr.status = status;
+            dr.done = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + kWsRouteOffset);
+        }
+        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H), status,
+                                 fused_routing ? &dr : nullptr) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (!fused_routing) {
+            if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
+            if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active,
+                                r.disp_scratch, status, st) != cudaSuccess)
+                return MOE_ERR_CUDA;
+        }
+        return run_gemv(mc, b, true, st);
+    }
+    GemmBufs b;
+    carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
+    // prefill routing: the top-k launch also counts each CTA's picks per expert (at most 64 CTAs,
+    // so the count table always fits: 64 * E <= 16384 for E <= 256), and the dispatch is the
+    // scatter alone, writing the tile list too (no count, scan or tile launches)
+    const int tpw = counted_tokens_per_warp(T, W->E);
+    const int rblk = counted_ctas(T, tpw);
+    if (!dispatch_counted_supported(rblk, W->E)) return MOE_ERR_UNSUPPORTED;
+    // tensor-core logits in up to 4 K ranges (more CTAs issuing copies), summed by the top-k
+    int parts = 1;
+    if (router_tc_supported(x, W_r, g, W->H, W->E)) {
+        parts = router_tc_ksplit(W->H);
+        if (launch_router_logits_tc(x, W_r, g, T, W->H, W->E, r.logits, status, st, parts) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    } else if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) !=
+               cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
+    if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st, parts) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_dispatch_counted(ids, T * k, W->E, kCountedWarps * tpw * k, rblk, r.route_cnt, r.counts, r.offsets,
+                                r.perm, r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return run_gemm(mc, b, st, true);
 }
 
 }  // namespace
@@ -430,78 +519,8 @@ size_t moe_workspace_size(int T, int E, int k, int H, int I, int I_sh) {
 int moe_layer_forward(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r, const moe_experts* W,
                       const moe_shared* sh, int T, int k, float* y, int32_t* topk_ids_out, float* topk_w_out, int arm,
                       void* ws, size_t ws_bytes, moe_stream_t stream) {
-    if (int s = check_experts(W)) return s;
-    if (int s = check_shared(sh)) return s;
-    if (T < 0 || k < 1 || k > MOE_MAX_K || k > W->E) return MOE_ERR_INVALID_ARG;
-    if (T == 0) return MOE_OK;
-    if (!x || !W_r || !y || !ws || !aligned16(x) || !aligned16(W_r) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
-    if (residual && (reinterpret_cast<uintptr_t>(residual) & 7u)) return MOE_ERR_INVALID_ARG;
-    if (reinterpret_cast<uintptr_t>(ws) % kWsAlign) return MOE_ERR_INVALID_ARG;
-    const int I_sh = sh ? sh->I_sh : 0;
-    if (ws_bytes < moe_workspace_size(T, W->E, k, W->H, W->I, I_sh)) return MOE_ERR_INVALID_ARG;
-    const int a = choose_arm(arm, T, k, W->E, W->H, W->I, I_sh);
-    if (a < 0) return arm == MOE_ARM_AUTO || arm == MOE_ARM_GEMV || arm == MOE_ARM_GEMM ? MOE_ERR_UNSUPPORTED
-                                                                                      : MOE_ERR_INVALID_ARG;
-    if (int s = check_device()) return s;
-    cudaStream_t st = S(stream);
-    int* status = static_cast<int*>(ws);
-    Carver c(ws);
-    Routing r;
-    carve_routing(c, T, W->E, k, r);
-    int32_t* ids = topk_ids_out ? topk_ids_out : r.ids;
-    float* w = topk_w_out ? topk_w_out : r.w;
-    const uint16_t* g = sh ? sh->g : nullptr;
-    const int ld = W->E + (g ? 1 : 0);
-    MlpCall mc{};
-    mc.x = x; mc.T = T; mc.k = k; mc.W = W; mc.sh = sh; mc.logits = r.logits; mc.logit_ld = ld;
-    mc.offsets = r.offsets; mc.perm = r.perm; mc.inv = r.inv; mc.active = r.active; mc.n_active = r.n_active;
-    mc.topk_w = w; mc.residual = residual; mc.rows_out = nullptr; mc.y = y; mc.status = status;
-    if (a == MOE_ARM_GEMV) {
-        GemvBufs b;
-        carve_gemv(c, T, k, W->H, W->I, I_sh, b);
-        // decode batches: 3 launches -- logits + x quantisation + top-k + dispatch, gate/up, down + combine
-        const bool fused_routing = T <= 32;
-        DecodeRoute dr;
-        if (fused_routing) {
-            dr.k = k; dr.ids = ids; dr.w = w; dr.counts = r.counts; dr.offsets = r.offsets; dr.perm = r.perm;
-            dr.inv = r.inv; dr.active = r.active; dr.n_active = r.n_active; dr.status = status;
-            dr.done = reinterpret_cast<int*>(reinterpret_cast<char*>(status) + kWsRouteOffset);
-        }
-        if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, b.xq, b.xmeta, act_gld(W->H), status,
-                                 fused_routing ? &dr : nullptr) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        if (!fused_routing) {
-            if (launch_router_topk(r.logits, false, ld, T, W->E, k, ids, w, st) != cudaSuccess) return MOE_ERR_CUDA;
-            if (launch_dispatch(ids, T * k, W->E, r.counts, r.offsets, r.perm, r.inv, r.active, r.n_active,
-                                r.disp_scratch, status, st) != cudaSuccess)
-                return MOE_ERR_CUDA;
-        }
-        return run_gemv(mc, b, true, st);
-    }
-    GemmBufs b;
-    carve_gemm(c, T, k, W->E, W->H, W->I, I_sh, b);
-    // prefill routing: the top-k launch also counts each CTA's picks per expert (at most 64 CTAs,
-    // so the count table always fits: 64 * E <= 16384 for E <= 256), and the dispatch is the
-    // scatter alone, writing the tile list too (no count, scan or tile launches)
-    const int tpw = counted_tokens_per_warp(T, W->E);
-    const int rblk = counted_ctas(T, tpw);
-    if (!dispatch_counted_supported(rblk, W->E)) return MOE_ERR_UNSUPPORTED;
-    // tensor-core logits in up to 4 K ranges (more CTAs issuing copies), summed by the top-k
-    int parts = 1;
-    if (router_tc_supported(x, W_r, g, W->H, W->E)) {
-        parts = router_tc_ksplit(W->H);
-        if (launch_router_logits_tc(x, W_r, g, T, W->H, W->E, r.logits, status, st, parts) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    } else if (launch_router_logits(x, W_r, g, T, W->H, W->E, r.logits, st, nullptr, nullptr, 0, status) !=
-               cudaSuccess) {
-        return MOE_ERR_CUDA;
-    }
-    if (launch_router_topk_counted(r.logits, ld, T, W->E, k, tpw, ids, w, r.route_cnt, st, parts) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (launch_dispatch_counted(ids, T * k, W->E, kCountedWarps * tpw * k, rblk, r.route_cnt, r.counts, r.offsets,
-                                r.perm, r.inv, r.active, r.n_active, status, b.tiles, b.n_tiles, st) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    return run_gemm(mc, b, st, true);
+    return layer_forward(x, residual, W_r, W, sh, T, k, y, topk_ids_out, topk_w_out, arm, ws, ws_bytes, stream,
+                         nullptr);
 }
 
 int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, float eps, uint16_t* y_norm,
@@ -524,11 +543,9 @@ int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const ui
     if (T > 0 && (!norm_gamma || !y_norm || (reinterpret_cast<uintptr_t>(norm_gamma) & 7u) ||
                   (reinterpret_cast<uintptr_t>(y_norm) & 7u)))
         return MOE_ERR_INVALID_ARG;
-    if (int s = moe_layer_forward(x, residual, W_r, W, sh, T, k, y, topk_ids_out, topk_w_out, arm, ws, ws_bytes,
-                                  stream))
-        return s;
-    if (T == 0) return MOE_OK;
-    return status_of(launch_rmsnorm(y, norm_gamma, T, W->H, eps, y_norm, S(stream)));
+    const NormOut norm{norm_gamma, eps, y_norm};
+    return layer_forward(x, residual, W_r, W, sh, T, k, y, topk_ids_out, topk_w_out, arm, ws, ws_bytes, stream,
+                         &norm);
 }
 
 }  // extern "C"

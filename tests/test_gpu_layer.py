@@ -225,21 +225,40 @@ def test_rmsnorm_stage(moe, T, H):
     _check_norm(y, gamma, 1e-6, out.cpu().numpy())
 
 
-@pytest.mark.parametrize("name", ["tiny", "qwen3_30b_decode_t16"])
-def test_layer_forward_norm(moe, name):
+@pytest.mark.parametrize("name,arm,over", [
+    # GEMV arm: the norm's own launch after the down projection with the folded combine
+    ("tiny", 0, {}),
+    ("qwen3_30b_decode_t1", 0, {}),
+    ("qwen3_30b_decode_t16", 0, {}),
+    ("tiny", 1, {"T": 32, "I_sh": 64}),               # shared expert
+    ("tiny", 1, {"T": 13, "H": 6144}),
+    ("tiny", 1, {"T": 3, "H": 24576, "residual": False}),  # the largest H
+    # tensor arm: the combine norms its rows
+    ("tiny", 2, {"T": 40}),
+    ("qwen15_prefill_t512", 2, {"T": 300}),           # ragged last 128-row tile
+])
+def test_layer_forward_norm(moe, name, arm, over):
     """The layer with its RMSNorm output: y identical to the plain layer call, y_norm the
-    oracle's RMSNorm of that y."""
+    oracle's RMSNorm of that y and, bit for bit, the standalone norm's output on that y (the
+    combine that norms its rows keeps the standalone kernel's order); a repeated call gives
+    the same bits."""
     import torch
-    inp = wk.layer(name)
+    inp = wk.layer(name, **over)
     x, r, W_r, E, S = wk.upload(inp)
     wl = inp.wl
     layer = moe.MoeLayer(W_r, E, S, wl.k, wl.T)
     gamma = gen.bf16_bits(gen.rng(22, wl.H).normal(1.0, 0.1, size=wl.H).astype(np.float32))
     gd = wk.dev(gamma.view(np.int16), torch.bfloat16)
-    y0 = layer.forward(x, r).clone()
+    y0 = layer.forward(x, r, arm=arm).clone()
     y = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda"))
     yn = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda"))
-    layer.forward(x, r, y=y, norm_gamma=gd, eps=1e-5, y_norm=yn)
+    layer.forward(x, r, y=y, norm_gamma=gd, eps=1e-5, y_norm=yn, arm=arm)
+    yn_stage = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda"))
+    moe.moe_rmsnorm(y, gd, 1e-5, yn_stage)
+    yn2 = wk.poison(torch.empty((wl.T, wl.H), dtype=torch.int16, device="cuda"))
+    layer.forward(x, r, y=y, norm_gamma=gd, eps=1e-5, y_norm=yn2, arm=arm)
     torch.cuda.synchronize()
     assert torch.equal(y, y0)
+    assert torch.equal(yn, yn_stage)
+    assert torch.equal(yn2, yn)
     _check_norm(y.cpu().numpy(), gamma, 1e-5, yn.cpu().numpy())
