@@ -396,8 +396,10 @@ def measure_decode(torch, moe, args, seed0):
                          "p10_us": s["p10_us"], "p90_us": s["p90_us"], "tokens_per_s": T / (us * 1e-6),
                          "mean_distinct_experts": nd, "layer_bytes": layer_bytes,
                          "hbm_frac": layer_bytes / (us * 1e-6) / 1e9 / hbm}
+        kern = kernel_times(torch, moe, step, n)
+        out[f"T={T}"]["kernels_us_per_step"] = {nm: 1e3 * v[0] / n for nm, v in kern.items()}
         if T == 16:
-            kern16 = kernel_times(torch, moe, step, n)
+            kern16 = kern
             kb = {"gateup_gemv": nd * (2 * I * H // 2 + 2 * I * (H // 32) * 2) + T * H * 2 + T * (H // 32) * 8
                   + T * k * I * 4,
                   "down_gemv_combine": nd * (H * I // 2 + H * (I // 32) * 2) + T * k * I * 2
@@ -408,7 +410,6 @@ def measure_decode(torch, moe, args, seed0):
                     kus = 1e3 * kern16[name][0] / max(kern16[name][1], 1)
                     kf[name] = {"us": kus, "bytes": b, "hbm_frac": b / (kus * 1e-6) / 1e9 / hbm}
             out["T=16"]["kernels"] = kf
-            out["T=16"]["kernels_us_per_step"] = {nm: 1e3 * v[0] / n for nm, v in kern16.items()}
     del layers
     torch.cuda.empty_cache()
     return out

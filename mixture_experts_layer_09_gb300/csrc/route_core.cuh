@@ -30,6 +30,15 @@ template <>
 __device__ __forceinline__ float load_logit<CoherentF32>(const CoherentF32* p) {
     return __ldcg(reinterpret_cast<const float*>(p));
 }
+// fp32 logits staged in shared memory by the calling CTA
+struct SharedF32 {
+    float v;
+};
+static_assert(sizeof(SharedF32) == sizeof(float), "one logit per element");
+template <>
+__device__ __forceinline__ float load_logit<SharedF32>(const SharedF32* p) {
+    return p->v;
+}
 
 // VPT = values per lane = ceil(E / 32); expert index of (lane, j) is lane + 32 * j.
 // One warp selects the top-k of one logit row.  ids/w receive the row's k outputs; hist (shared

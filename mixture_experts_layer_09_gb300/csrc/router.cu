@@ -12,6 +12,8 @@
 // of the warp MoE router", warp-router commit).  Selection is k rounds of a warp argmax with
 // the lowest index winning a tie; weights are the fp32 softmax over all E logits renormalised
 // over the k picks; the picks are written in ascending expert id.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "quant.cuh"
@@ -241,63 +243,92 @@ __global__ void __launch_bounds__(256) router_topk_warp_kernel(const Tin* __rest
                             topk_w + static_cast<size_t>(t) * k, bias, renorm != 0, scale);
 }
 
-// Counted variant (prefill layer): kCountedWarps warps of tpw tokens each; the CTA's picks per
-// expert go to row blockIdx.x of the dispatch count table.
+// Counted variant (prefill layer): a CTA takes kCountedWarps * tpw consecutive tokens, in
+// rounds of kCountedWarps (warp w takes token w of a round); its picks per expert go to row
+// blockIdx.x of the dispatch count table.  The logit rows of rpr rounds at a time are staged in
+// shared memory by the whole CTA (coalesced, every load in flight): with K-split router logits
+// the partial planes are summed there, in plane order, and the sums also written back to plane 0
+// (the shared gate's logit is read from it later); each warp then selects from its staged row.
+constexpr int kCountedUnroll = 8;  // staged values per thread per batch (times the planes)
+
 template <int VPT>
-__global__ void __launch_bounds__(kCountedWarps * 32) router_topk_counted_kernel(float* logits, int ld, int T, int E, int k, int tpw,
-                                                                  int32_t* __restrict__ topk_ids,
-                                                                  float* __restrict__ topk_w, int* __restrict__ cta_cnt,
-                                                                  int parts) {
+__global__ void __launch_bounds__(kCountedWarps * 32) router_topk_counted_kernel(float* logits, int ld, int T, int E,
+                                                                                 int k, int tpw, int rpr,
+                                                                                 int32_t* __restrict__ topk_ids,
+                                                                                 float* __restrict__ topk_w,
+                                                                                 int* __restrict__ cta_cnt, int parts) {
+    extern __shared__ float rows_s[];  // [kCountedWarps * rpr][ld]
     __shared__ int hist[32 * VPT];
     for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-    const int c0 = blockIdx.x * (blockDim.x >> 5) * tpw;  // the CTA's first token
-    if (parts > 1) {
-        // the final logits (the shared gate included): the CTA's rows of the partial planes summed
-        // in plane order into plane 0, every thread several values with all their loads in flight
-        const size_t plane = static_cast<size_t>(T) * ld;
-        const int nval = (min(T, c0 + static_cast<int>(blockDim.x >> 5) * tpw) - c0) * ld;
-        float* base = logits + static_cast<size_t>(c0) * ld;
-        for (int i = threadIdx.x; i < nval; i += blockDim.x) {
-            float v[4];
+    const int w = threadIdx.x >> 5;
+    const int c0 = blockIdx.x * kCountedWarps * tpw;  // the CTA's first token
+    const int cend = min(T, c0 + kCountedWarps * tpw);
+    const size_t plane = static_cast<size_t>(T) * ld;
+    for (int j0 = 0; j0 < tpw; j0 += rpr) {
+        // rounds j0 .. j0 + rpr - 1: tokens [r0, r1), contiguous rows of the logits
+        const int r0 = min(cend, c0 + j0 * kCountedWarps);
+        const int r1 = min(cend, r0 + rpr * kCountedWarps);
+        const int nval = (r1 - r0) * ld;
+        float* base = logits + static_cast<size_t>(r0) * ld;
+        for (int i0 = 0; i0 < nval; i0 += kCountedUnroll * kCountedWarps * 32) {
+            float v[kCountedUnroll][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = (q < parts) ? __ldg(base + q * plane + i) : 0.f;
-            float sum = v[0];
+            for (int u = 0; u < kCountedUnroll; ++u) {
+                const int i = i0 + u * kCountedWarps * 32 + threadIdx.x;
 #pragma unroll
-            for (int q = 1; q < 4; ++q)
-                if (q < parts) sum += v[q];
-            base[i] = sum;
+                for (int q = 0; q < 4; ++q) v[u][q] = (i < nval && q < parts) ? __ldg(base + q * plane + i) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kCountedUnroll; ++u) {
+                const int i = i0 + u * kCountedWarps * 32 + threadIdx.x;
+                if (i < nval) {
+                    float sum = v[u][0];
+#pragma unroll
+                    for (int q = 1; q < 4; ++q)
+                        if (q < parts) sum += v[u][q];
+                    rows_s[i] = sum;
+                    if (parts > 1) base[i] = sum;
+                }
+            }
         }
         __syncthreads();
+        for (int r = 0; r < rpr; ++r) {
+            const int t = r0 + r * kCountedWarps + w;
+            if (t < r1)
+                topk_warp_row<SharedF32, VPT>(reinterpret_cast<const SharedF32*>(rows_s + (t - r0) * ld), E, k,
+                                              topk_ids + static_cast<size_t>(t) * k,
+                                              topk_w + static_cast<size_t>(t) * k, nullptr, true, 1.f, hist);
+        }
+        __syncthreads();  // the staged rows are replaced by the next rounds'
     }
-    const int t0 = c0 + (threadIdx.x >> 5) * tpw;
-    for (int t = t0; t < min(T, t0 + tpw); ++t) {
-        const float* row = logits + static_cast<size_t>(t) * ld;
-        if (parts > 1)
-            topk_warp_row<CoherentF32, VPT>(reinterpret_cast<const CoherentF32*>(row), E, k,
-                                            topk_ids + static_cast<size_t>(t) * k, topk_w + static_cast<size_t>(t) * k,
-                                            nullptr, true, 1.f, hist);
-        else
-            topk_warp_row<float, VPT>(row, E, k, topk_ids + static_cast<size_t>(t) * k,
-                                      topk_w + static_cast<size_t>(t) * k, nullptr, true, 1.f, hist);
-    }
-    __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) cta_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
+}
+
+// Rounds staged at once: as many as fit kCountedStageBytes of shared memory (at least one).
+constexpr int kCountedStageBytes = 48 * 1024;
+static int counted_rounds_per_stage(int tpw, int ld) {
+    const int fit = kCountedStageBytes / (kCountedWarps * ld * static_cast<int>(sizeof(float)));
+    return std::max(1, std::min(tpw, fit));
 }
 
 cudaError_t launch_router_topk_counted(float* logits, int ld, int T, int E, int k, int tpw, int32_t* ids, float* w,
                                        int* cta_cnt, cudaStream_t st, int parts) {
     if (T == 0) return cudaSuccess;
+    if (parts < 1 || parts > 4) return cudaErrorInvalidValue;
     const int vpt = (E + 31) / 32;
+    const int rpr = counted_rounds_per_stage(tpw, ld);
+    const size_t smem = static_cast<size_t>(kCountedWarps) * rpr * ld * sizeof(float);
+    if (smem > static_cast<size_t>(kCountedStageBytes)) return cudaErrorInvalidValue;
     const dim3 grid((T + kCountedWarps * tpw - 1) / (kCountedWarps * tpw)), block(kCountedWarps * 32);
     KernelScope ks_("router_topk+count", st);
     switch (vpt) {
 #define MOE_TOPKC_CASE(V) \
-    case V:                                                                                                    \
-        return launch_pdl(router_topk_counted_kernel<V>, grid, block, 0, st, logits, ld, T, E, k, tpw, ids, w, \
-                          cta_cnt, parts);
+    case V:                                                                                                   \
+        return launch_pdl(router_topk_counted_kernel<V>, grid, block, smem, st, logits, ld, T, E, k, tpw, rpr, ids, \
+                          w, cta_cnt, parts);
         MOE_TOPKC_CASE(1)
         MOE_TOPKC_CASE(2)
         MOE_TOPKC_CASE(3)

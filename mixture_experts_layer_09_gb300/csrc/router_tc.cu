@@ -46,8 +46,6 @@ __host__ __device__ inline int g_bytes(int H, bool has_g) { return has_g ? ((H *
 }  // namespace
 
 __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_constant__ RouterTcArgs p) {
-    pdl_wait();
-    pdl_trigger();
     const int t0 = blockIdx.x * RM;
     const int ncols = p.E + (p.g ? 1 : 0);
     const int nk = p.H / RK / p.ksplit;          // K-steps of this CTA's range
@@ -79,11 +77,18 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
         for (int i = threadIdx.x; i < p.H / 8; i += blockDim.x)
             reinterpret_cast<uint4*>(gbuf)[i] = ldg_nc(p.g + static_cast<size_t>(i) * 8);
     }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&p.tm_x);
+        prefetch_tmap(&p.tm_w);
+    }
     if (warp == 1) tmem_alloc(tmem_slot, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // everything above reads only the router weights: it overlaps the previous launch's tail
+    pdl_wait();
+    pdl_trigger();
 
     if (warp == 0) {
         // ---------------- producer: token tile + router rows by TMA, gate row by hand
@@ -152,22 +157,31 @@ __global__ void __launch_bounds__(192, 1) router_logits_tc_kernel(const __grid_c
             }
         }
     } else {
-        // ---------------- epilogue: lane quadrant q holds tokens t0 + 32q .. t0 + 32q + 31
+        // ---------------- epilogue: lane quadrant q holds tokens t0 + 32q .. t0 + 32q + 31.
+        // Each 16-column chunk goes through shared memory (stage 0, idle once the accumulator is
+        // final), so that the stores run along the rows of the logits rather than down a column.
         bool go = __all_sync(0xffffffffu, mbar_wait(accum, 0, abort_flag, p.status, 23));
+        go = named_barrier_or(1, 128, !go) ? false : go;  // the four epilogue warps agree
         if (go) {
             tc_fence_after();
             const int q = warp & 3;
-            const int t = t0 + q * 32 + lane;
+            const int et = threadIdx.x - 64;  // 0 .. 127
             const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            float* stg = reinterpret_cast<float*>(smem);  // [128][17]
+            float* out = p.logits + (static_cast<size_t>(blockIdx.y) * p.T + t0) * p.ld;
+            const int nrow = min(RM, p.T - t0);
             for (int c0 = 0; c0 < ncols; c0 += 16) {
                 float v[16];
                 tmem_ld16(tbase + c0, v);
-                if (t < p.T) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c0 + j < ncols)
-                            p.logits[(static_cast<size_t>(blockIdx.y) * p.T + t) * p.ld + c0 + j] = v[j];
+                for (int j = 0; j < 16; ++j) stg[(q * 32 + lane) * 17 + j] = v[j];
+                named_barrier(1, 128);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int i = et + 128 * m, row = i >> 4, col = i & 15;
+                    if (row < nrow && c0 + col < ncols) out[static_cast<size_t>(row) * p.ld + c0 + col] = stg[row * 17 + col];
                 }
+                named_barrier(1, 128);
             }
         }
     }
