@@ -78,8 +78,9 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_count_kernel(
     }
 }
 
-// Phase 2: stable scatter.  Thread e (one per expert) reads column e of the count table: the
-// expert's total and the part of it counted by the CTAs before this one; the totals' exclusive
+// Phase 2: stable scatter.  The CTA loads the whole count table into shared memory (coalesced,
+// sixteen loads in flight per thread), then sums each expert's column in parallel parts: the
+// expert's total and the part of it counted by the CTAs before this one.  The totals' exclusive
 // scan over the experts gives the bucket offsets, which CTA 0 also writes out with the counts
 // and the active-expert list.
 __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
@@ -88,24 +89,50 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     int* status, int* tiles, int* n_tiles) {
     pdl_wait();
     pdl_trigger();
-    extern __shared__ int hist[];  // [kBigWarps][E]
+    extern __shared__ int hist[];  // [kBigWarps][E] | the count table [nblk][E]
+    int* tbl = hist + kBigWarps * E;
     __shared__ int scratch[9];
     __shared__ int base_e[MOE_MAX_E];
+    __shared__ int part_tot[kBigWarps * 32], part_bef[kBigWarps * 32];
     const int w = threadIdx.x >> 5;
     for (int i = threadIdx.x; i < kBigWarps * E; i += blockDim.x) hist[i] = 0;
+    const int nt = nblk * E;
+    for (int i0 = 0; i0 < nt; i0 += 16 * kBigWarps * 32) {
+        int v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = i0 + u * kBigWarps * 32 + static_cast<int>(threadIdx.x);
+            v[u] = i < nt ? __ldg(cta_cnt + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = i0 + u * kBigWarps * 32 + static_cast<int>(threadIdx.x);
+            if (i < nt) tbl[i] = v[u];
+        }
+    }
+    __syncthreads();
+    const int P = kBigWarps * 32 / E;  // threads per column (E <= 256)
+    {
+        const int e = threadIdx.x % E, q = threadIdx.x / E;
+        if (q < P) {
+            int tot = 0, bef = 0;
+            for (int r = q; r < nblk; r += P) {
+                const int c = tbl[r * E + e];
+                tot += c;
+                if (r < static_cast<int>(blockIdx.x)) bef += c;
+            }
+            part_tot[q * E + e] = tot;
+            part_bef[q * E + e] = bef;
+        }
+    }
+    __syncthreads();
     {
         const int e = threadIdx.x;
         int total = 0, before = 0;
         if (e < E) {
-            for (int r0 = 0; r0 < nblk; r0 += 4) {
-                int v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = (r0 + u < nblk) ? __ldg(cta_cnt + static_cast<size_t>(r0 + u) * E + e) : 0;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    total += v[u];
-                    if (r0 + u < static_cast<int>(blockIdx.x)) before += v[u];
-                }
+            for (int q = 0; q < P; ++q) {
+                total += part_tot[q * E + e];
+                before += part_bef[q * E + e];
             }
         }
         int sum, nact;
@@ -159,6 +186,17 @@ __global__ void __launch_bounds__(kBigWarps * 32) dispatch_scatter_kernel(
     warp_walk(ids, begin, end, E, hist + w * E, 1, perm, inv, status);
 }
 
+// Shared memory of the scatter: the per-warp histograms and the whole count table.
+static size_t scatter_smem(int nblk, int E) {
+    return (static_cast<size_t>(kBigWarps) + nblk) * E * sizeof(int);
+}
+static cudaError_t scatter_attr() {
+    static const cudaError_t once = cudaFuncSetAttribute(
+        dispatch_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>((static_cast<size_t>(kBigWarps) * MOE_MAX_E + kMaxTableInts) * sizeof(int)));
+    return once;
+}
+
 size_t dispatch_scratch_bytes(int n, int E) {
     if (n <= kSmallSlots) return 0;
     const int spc = slots_per_cta(n, E);
@@ -188,8 +226,11 @@ cudaError_t launch_dispatch(const int32_t* ids, int n, int E, int32_t* counts, i
         if (e != cudaSuccess) return e;
     }
     {
+        cudaError_t e = scatter_attr();
+        if (e != cudaSuccess) return e;
         KernelScope ks_("dispatch_scatter", st);
-        return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), smem, st, ids, n, E, spc, nblk,
+        return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), scatter_smem(nblk, E), st, ids, n,
+                          E, spc, nblk,
                           static_cast<const int*>(cnt), counts, offsets, active, n_active, perm, inv, status,
                           static_cast<int*>(nullptr), static_cast<int*>(nullptr));
     }
@@ -203,8 +244,10 @@ cudaError_t launch_dispatch_counted(const int32_t* ids, int n, int E, int spc, i
                                     int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* active,
                                     int32_t* n_active, int* status, int* tiles, int* n_tiles, cudaStream_t st) {
     if (spc % kBigWarps || !dispatch_counted_supported(nblk, E)) return cudaErrorInvalidValue;
+    cudaError_t e = scatter_attr();
+    if (e != cudaSuccess) return e;
     KernelScope ks_("dispatch_scatter+tiles", st);
-    return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), kBigWarps * E * sizeof(int), st, ids,
+    return launch_pdl(dispatch_scatter_kernel, dim3(nblk), dim3(kBigWarps * 32), scatter_smem(nblk, E), st, ids,
                       n, E, spc, nblk, cta_cnt, counts, offsets, active, n_active, perm, inv, status, tiles, n_tiles);
 }
 
