@@ -307,8 +307,9 @@ __global__ void __launch_bounds__(kCountedWarps * 32) router_topk_counted_kernel
     for (int e = threadIdx.x; e < E; e += blockDim.x) cta_cnt[static_cast<size_t>(blockIdx.x) * E + e] = hist[e];
 }
 
-// Rounds staged at once: as many as fit kCountedStageBytes of shared memory (at least one).
-constexpr int kCountedStageBytes = 48 * 1024;
+// Rounds staged at once: as many as fit kCountedStageBytes of shared memory (at least one; with
+// the kernel's static histogram this stays under the 48 KB a launch gets without opting in).
+constexpr int kCountedStageBytes = 40 * 1024;
 static int counted_rounds_per_stage(int tpw, int ld) {
     const int fit = kCountedStageBytes / (kCountedWarps * ld * static_cast<int>(sizeof(float)));
     return std::max(1, std::min(tpw, fit));

@@ -77,10 +77,12 @@ def test_k32_of_256_experts(moe, arm):
     (1, 2048, 128, 64, 8, 128),      # one token on the tensor arm (4 K ranges, one top-k CTA)
     (77, 3136, 192, 33, 3, 64),      # 49 K-steps: one K range; odd E
     (4100, 1024, 64, 16, 2, 0),      # above 64 * 16 tokens: 8 tokens per top-k warp, 33 count rows
+    (4100, 256, 64, 256, 8, 0),      # E=256: the top-k stages its rows in four rounds of 2 tokens per warp
+    (2000, 512, 64, 255, 4, 64),     # E=255 + the shared gate: 256-wide logit rows, 63 count rows
 ])
 def test_tensor_arm_routing_shapes(moe, T, H, I, E, k, I_sh):
     """The tensor arm's routing at shapes that take its other branches: the router's partial
-    planes (1, 2 or 4), the counted top-k with several tokens per warp, the scatter's count table
-    with a ragged last CTA, and the tile list it writes."""
+    planes (1, 2 or 4), the counted top-k with several tokens per warp and several staging rounds
+    per CTA, the scatter's count table with a ragged last CTA, and the tile list it writes."""
     wl = gen.Workload("route", T, H, I, E, k, I_sh=I_sh, seed=9)
     _check(moe, wk.enforce_margin_x(gen.draw_layer(wl)), 2)
