@@ -285,12 +285,24 @@ __device__ __forceinline__ void combine_flush(const GemvArgs& p, int cb, int cnt
     if (*last_flag) {
         __threadfence();
         const int H = p.H;
+        // every term's load is issued before the sum (eight slots at a time), and the adds keep
+        // the order shared, slots 0..k-1, residual
         for (int idx = threadIdx.x; idx < p.T * 32; idx += kCW * 32) {
             const int tt = idx >> 5, nn = cb * 32 + (idx & 31);
-            float y = (p.sh_I > 0) ? __ldcg(p.sh_term + static_cast<size_t>(tt) * H + nn) : 0.f;
-            for (int j = 0; j < p.k; ++j) y += __ldcg(p.slot_term + (static_cast<size_t>(tt) * p.k + j) * H + nn);
-            if (p.residual) y += bf16_to_f32(p.residual[static_cast<size_t>(tt) * H + nn]);
-            p.y[static_cast<size_t>(tt) * H + nn] = y;
+            const size_t at = static_cast<size_t>(tt) * H + nn;
+            float y = (p.sh_I > 0) ? __ldcg(p.sh_term + at) : 0.f;
+            const float res = p.residual ? bf16_to_f32(p.residual[at]) : 0.f;
+            const float* slots = p.slot_term + static_cast<size_t>(tt) * p.k * H + nn;
+            for (int j0 = 0; j0 < p.k; j0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = (j0 + u < p.k) ? __ldcg(slots + static_cast<size_t>(j0 + u) * H) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (j0 + u < p.k) y += v[u];
+            }
+            if (p.residual) y += res;
+            p.y[at] = y;
         }
         if (threadIdx.x == 0) p.col_counter[cb] = 0;  // ready for the next call
     }
