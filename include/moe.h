@@ -255,7 +255,7 @@ MOE_API int moe_rmsnorm(const float* y, const uint16_t* gamma, int T, int H, flo
 
 /* moe_layer_forward with the RMSNorm of its y: y receives the layer output, y_norm its RMSNorm
  * with norm_gamma bf16 [H] and eps, bit-identical to moe_rmsnorm on that y.  The tensor arm's
- * combine norms each row as it writes it (no extra launch, no second read of y); the GEMV arm,
+ * combine norms each row as it writes it (no extra launch, no second pass over y in HBM); the GEMV arm,
  * whose combine is folded into the down projection, runs the norm as one more launch on the
  * same stream. */
 MOE_API int moe_layer_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* W_r,
